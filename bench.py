@@ -1,0 +1,323 @@
+"""Benchmark of exact attention on one GB300: forward + backward at B=1, H=16, N=8192, d=128 (bf16).
+
+One step = one forward (fa_fwd) and one backward (fa_bwd) over the same seeded synthetic batch, the
+whole hot path.  Prints one JSON line (see ``main``).  ``--impl reference`` times the fp64 CPU oracle
+on the host cores instead (a bounded sample of the same workload per step).
+"""
+from __future__ import annotations
+
+import os
+
+# The oracle's BLAS uses every host core; set before numpy is imported anywhere.
+_NCPU = os.cpu_count() or 1
+for _v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS"):
+    os.environ.setdefault(_v, str(_NCPU))
+
+import argparse
+import json
+import math
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+import fa_inputs
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"bf16_tflops": p["bf16_tflops"], "bf16_tflops_sustained": p.get("bf16_tflops_sustained"),
+                "hbm_gbs": p["hbm_gbs"], "source": "measured"}
+    return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _oracle_sample(w, rows: int, inp):
+    """fp64 oracle forward + backward for one head with `rows` query rows against all N keys."""
+    import oracle
+    q = inp["q"][:1, :1, :rows].double().numpy()
+    k = inp["k"][:1, :1].double().numpy()
+    v = inp["v"][:1, :1].double().numpy()
+    do = inp["do"][:1, :1, :rows].double().numpy()
+    t0 = time.perf_counter()
+    oracle.forward(q, k, v, w.scale)
+    oracle.backward(q, k, v, do, w.scale)
+    dt = time.perf_counter() - t0
+    flops = 14.0 * rows * w.N * w.d
+    return flops, dt
+
+
+def _cpu_meta(rows, w):
+    return {"kind": "oracle", "cores": _NCPU,
+            "sample": f"fp64 oracle forward+backward of head 0 with {rows} of {w.N} query rows against all "
+                      f"{w.N} keys (d={w.d}); flops counted as 14*rows*N*d"}
+
+
+def run_reference(args, w):
+    rank, world, _ = _dist_env()
+    if rank != 0:
+        return 0
+    inp = fa_inputs.workload_inputs(w, with_grad=True)
+    rows = args.oracle_rows
+    for _ in range(args.warmup):
+        _oracle_sample(w, rows, inp)
+    total_f, total_t = 0.0, 0.0
+    for _ in range(args.steps):
+        f, t = _oracle_sample(w, rows, inp)
+        total_f += f
+        total_t += t
+    tflops = total_f / total_t / 1e12
+    meta = _cpu_meta(rows, w)
+    meta["value"] = tflops
+    meta["unit"] = "TFLOP/s"
+    line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total_t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(w, world), "cpu_baseline": meta,
+            "e2e": {"value": tflops, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+METRIC = "attention TFLOP/s fwd and fwd+bwd vs BF16 tensor peak (N=8192, d=128, 1xGB300)"
+
+
+def _config(w, world):
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
+            "step": "fa_fwd + fa_bwd", "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+            "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"}
+
+
+def run_ours(args, w):
+    import exact_io_aware_17_gb300 as fa
+
+    rank, world, local = _dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    fa.load_library()
+
+    inp_cpu = fa_inputs.workload_inputs(w, with_grad=True)
+    q, k, v, do = (inp_cpu[n].to(dev) for n in ("q", "k", "v", "do"))
+    B, H, N, d = w.B, w.H, w.N, w.d
+    o = torch.empty_like(q)
+    lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        fa.fa_fwd(q, k, v, w.scale, o, lse, stream=stream)
+        fa.fa_bwd(q, k, v, o, do, lse, w.scale, dq, dk, dv, ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    fa.fa_check_status(stream)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xff)                      # evict the previous step's data from L2 (untimed)
+        ev[i][0].record(stream)
+        fa.fa_fwd(q, k, v, w.scale, o, lse, stream=stream)
+        ev[i][1].record(stream)
+        fa.fa_bwd(q, k, v, o, do, lse, w.scale, dq, dk, dv, ws, stream=stream)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t_wall
+    clk = clocks.stop()
+    fa.fa_check_status(stream)
+
+    fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    step_ms = sum(fwd_ms) / args.steps + sum(bwd_ms) / args.steps
+    if world > 1:
+        t = torch.tensor([step_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_ms = float(t.item())
+    total_flops = (w.fwd_flops() + w.bwd_flops()) * world
+    value = total_flops / (step_ms * 1e-3) / 1e12
+    fwd_avg = sum(fwd_ms) / args.steps
+    bwd_avg = sum(bwd_ms) / args.steps
+    fwd_tflops = w.fwd_flops() / (fwd_avg * 1e-3) / 1e12
+    bwd_tflops = w.bwd_flops() / (bwd_avg * 1e-3) / 1e12
+    peaks = _peaks()
+    peak = peaks["bf16_tflops"]
+
+    # End to end through the public API: pinned host inputs in, gradients and O back to pinned host memory.
+    host_in = {n: inp_cpu[n].pin_memory() for n in ("q", "k", "v", "do")}
+    host_out = {n: torch.empty_like(inp_cpu["q"]).pin_memory() for n in ("o", "dq", "dk", "dv")}
+    host_lse = torch.empty(B, H, N, dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
+            t.copy_(host_in[n], non_blocking=True)
+        step()
+        for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
+            host_out[n].copy_(t, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    e2e_steps = max(3, args.steps // 2)
+    e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    elt = q.element_size() * q.numel()
+    h2d = 4 * elt
+    d2h = 4 * elt + host_lse.numel() * 4
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded iid N(0,1), bf16)",
+        "config": _config(w, world),
+        "fwd": {"ms": fwd_avg, "tflops": fwd_tflops, "frac_of_peak": fwd_tflops / peak},
+        "bwd": {"ms": bwd_avg, "tflops": bwd_tflops, "frac_of_peak": bwd_tflops / peak},
+        "fwd_bwd_frac_of_peak": value / world / peak,
+        "wall_s_timed_region": wall,
+        "clocks": clk,
+        "gpu_launches": args.steps * LAUNCHES_PER_STEP,
+        "e2e": {"value": (w.fwd_flops() + w.bwd_flops()) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+    }
+    line["roofline"] = _roofline(w, fwd_avg, bwd_avg, peaks)
+    if rank == 0 and not args.no_cpu_baseline:
+        rows = args.oracle_rows
+        f, t = _oracle_sample(w, rows, inp_cpu)
+        meta = _cpu_meta(rows, w)
+        meta.update({"value": f / t / 1e12, "unit": "TFLOP/s", "seconds": t})
+        line["cpu_baseline"] = meta
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+# Kernels launched per step: the forward kernel, and the backward's row-term, main and dQ kernels.
+LAUNCHES_PER_STEP = 4
+
+
+def _roofline(w, fwd_ms, bwd_ms, peaks):
+    """Roofline of the dominant kernel (the one with the larger share of the step)."""
+    if bwd_ms >= fwd_ms:
+        name, flops, ms = "backward", w.bwd_flops(), bwd_ms
+    else:
+        name, flops, ms = "forward", w.fwd_flops(), fwd_ms
+    achieved = flops / (ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"]
+    return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "peak_source": f"{peaks['source']} burst bf16 (cuBLAS)", "traffic": None}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=fa_inputs.HEADLINE, choices=sorted(fa_inputs.WORKLOADS))
+    ap.add_argument("--oracle-rows", type=int, default=512)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    w = fa_inputs.WORKLOADS[args.workload]
+    if not w.backward:
+        raise SystemExit("the bench step is forward + backward: pick a workload with a backward pass")
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

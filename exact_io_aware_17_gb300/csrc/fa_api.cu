@@ -1,0 +1,155 @@
+// C entry points of libfa.so: argument checks, workspace layout, dispatch to the kernels.
+// The declarations and their contracts are in include/fa.h.
+
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+
+#include "fa_internal.h"
+
+namespace fa {
+
+static thread_local char g_last_error[512] = "";
+
+fa_status set_error(fa_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+BwdWorkspace bwd_workspace_layout(const Shape& s) {
+    BwdWorkspace w;
+    const size_t rows = (size_t)s.rows();
+    w.dq_acc = 0;
+    w.row_d = round256(rows * (size_t)s.d * sizeof(float));
+    w.lse2 = w.row_d + round256(rows * sizeof(float));
+    w.total = w.lse2 + round256(rows * sizeof(float));
+    return w;
+}
+
+cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows) {
+    static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+    if (!encode) {
+        cudaDriverEntryPointQueryResult qres;
+        void* fn = nullptr;
+        cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &qres);
+        if (e != cudaSuccess) return e;
+        if (qres != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+        encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
+    }
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+    cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Common checks of every entry point; returns FA_OK or the error (message already recorded).
+static fa_status check_shape(const char* fn, int B, int H, int N, int d, float scale) {
+    if (B < 1 || H < 1 || N < 1 || d < 1)
+        return set_error(FA_ERR_INVALID_ARG, "%s: B, H, N, d must be >= 1 (got B=%d H=%d N=%d d=%d)", fn, B, H, N, d);
+    if ((int64_t)B * H > INT32_MAX || (int64_t)N * d > INT32_MAX)
+        return set_error(FA_ERR_INVALID_ARG, "%s: B*H and N*d must fit in int32", fn);
+    if (!isfinite(scale) || !(scale > 0.f))
+        return set_error(FA_ERR_INVALID_ARG, "%s: scale must be finite and > 0 (got %g)", fn, (double)scale);
+    return FA_OK;
+}
+
+static fa_status check_ptrs(const char* fn, const void* const* ptrs, const char* const* names, int n) {
+    for (int i = 0; i < n; ++i) {
+        if (!ptrs[i]) return set_error(FA_ERR_INVALID_ARG, "%s: %s is NULL", fn, names[i]);
+        if (!aligned16(ptrs[i])) return set_error(FA_ERR_INVALID_ARG, "%s: %s is not 16-byte aligned", fn, names[i]);
+    }
+    return FA_OK;
+}
+
+static fa_status launch_result(const char* fn, cudaError_t e) {
+    if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+    return FA_OK;
+}
+
+}  // namespace fa
+
+using namespace fa;
+
+extern "C" {
+
+const char* fa_last_error_string(void) { return g_last_error; }
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, void* stream) {
+    g_last_error[0] = 0;
+    fa_status st = check_shape("fa_fwd", B, H, N, d, scale);
+    if (st) return st;
+    const void* ptrs[] = {q, k, v, o, lse};
+    const char* names[] = {"q", "k", "v", "o", "lse"};
+    if ((st = check_ptrs("fa_fwd", ptrs, names, 5))) return st;
+    if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "fa_fwd: d must be 64 or 128 (got %d)", d);
+    Shape s{B, H, N, d};
+    return launch_result("fa_fwd", launch_fwd_tc(q, k, v, o, lse, s, scale, (cudaStream_t)stream));
+}
+
+fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                     int B, int H, int N, int d, float scale, void* stream) {
+    g_last_error[0] = 0;
+    fa_status st = check_shape("fa_fwd_f32", B, H, N, d, scale);
+    if (st) return st;
+    const void* ptrs[] = {q, k, v, o, lse};
+    const char* names[] = {"q", "k", "v", "o", "lse"};
+    if ((st = check_ptrs("fa_fwd_f32", ptrs, names, 5))) return st;
+    if (d > 128 || d % 4 != 0)
+        return set_error(FA_ERR_UNSUPPORTED, "fa_fwd_f32: d must be a multiple of 4 and <= 128 (got %d)", d);
+    Shape s{B, H, N, d};
+    return launch_result("fa_fwd_f32", launch_fwd_simt_f32(q, k, v, o, lse, s, scale, (cudaStream_t)stream));
+}
+
+size_t fa_bwd_workspace_size(int B, int H, int N, int d) {
+    if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+    return bwd_workspace_layout(Shape{B, H, N, d}).total;
+}
+
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, float scale,
+                 void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_error[0] = 0;
+    fa_status st = check_shape("fa_bwd", B, H, N, d, scale);
+    if (st) return st;
+    const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+    const char* names[] = {"q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv", "workspace"};
+    if ((st = check_ptrs("fa_bwd", ptrs, names, 10))) return st;
+    if ((uintptr_t)workspace & 255u) return set_error(FA_ERR_INVALID_ARG, "fa_bwd: workspace is not 256-byte aligned");
+    if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "fa_bwd: d must be 64 or 128 (got %d)", d);
+    Shape s{B, H, N, d};
+    BwdWorkspace w = bwd_workspace_layout(s);
+    if (workspace_bytes < w.total)
+        return set_error(FA_ERR_INVALID_ARG, "fa_bwd: workspace holds %zu bytes, needs %zu", workspace_bytes, w.total);
+    char* ws = (char*)workspace;
+    return launch_result("fa_bwd", launch_bwd_simt_bf16(q, k, v, o, dout, lse, dq, dk, dv, s, scale,
+                                                         (float*)(ws + w.row_d), (cudaStream_t)stream));
+}
+
+fa_status fa_check_status(void* stream) {
+    g_last_error[0] = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return set_error(FA_ERR_CUDA, "fa_check_status: %s", cudaGetErrorString(e));
+    int codes[] = {fwd_tc_read_and_clear_status(s), bwd_tc_read_and_clear_status(s)};
+    for (int c : codes) {
+        if (c < 0) return set_error(FA_ERR_CUDA, "fa_check_status: could not read the device status word");
+        if (c) return set_error(FA_ERR_TIMEOUT, "fa_check_status: a kernel gave up a bounded wait (code %d)", c);
+    }
+    return FA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,382 @@
+// bf16 attention forward on the sm_103a tensor cores (tcgen05 + TMA + tensor memory).
+//
+// Method ("账房先生的奔命：Flash Attention 与内存 I/O 革命" §六, Tiling + Online Softmax): a CTA owns two
+// tiles of 128 query rows (Q0, Q1) and streams K_j, V_j (128 keys each) through a shared-memory ring.
+// For every K/V block and both Q tiles:
+//     S = Q K_j^T                                   tcgen05.mma, fp32 in tensor memory (TMEM)
+//     m_new = max(m, rowmax(scale S))               one thread owns one row: no shuffles
+//     P = exp(scale S - m_new), l = a l + rowsum P  a = exp(m - m_new)
+//     O = a O + P V_j                               P goes back to TMEM as bf16 and feeds the MMA
+// and only O / l (bf16) and LSE = m + ln l (fp32) are written to global memory (the 技术解读 section of
+// "算珠楼的掌簿人": only the output and the statistics return to HBM).  The rescale by
+// exp(m_old - m_new) is the identity of the FlashAttention fable on ckw19810413.github.io (兩大核心魔法).
+//
+// Rescale skipping: the reference max used in the exponent is only moved when the row max grows by
+// more than 2^8 (in the log2 domain).  O and l always share that reference, so O / l and
+// m + ln l are unchanged; the skipped rescales only bound P by 256 instead of 1.
+//
+// Warp roles (320 threads): warps 0-3 own Q0's rows, warps 4-7 own Q1's rows (thread = row = TMEM
+// lane), warp 8 issues TMA loads, warp 9 allocates TMEM and issues the MMAs.  While one warpgroup
+// exponentiates its S tile the tensor cores run the other tile's MMAs.
+//
+// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "fa_internal.h"
+#include "fa_ptx.cuh"
+
+namespace fa {
+namespace {
+
+using namespace ptx;
+
+__device__ int g_fwd_status;
+
+constexpr int BM = 128;  // query rows per tile (MMA M, TMEM lanes)
+constexpr int BN = 128;  // keys per K/V block
+constexpr int kThreads = 320;
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kMaxStages = 4;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+struct FwdBarriers {
+    uint64_t q_full[2];
+    uint64_t k_full[kMaxStages];
+    uint64_t v_full[kMaxStages];
+    uint64_t kv_empty[kMaxStages];
+    uint64_t s_full[2];
+    uint64_t p_full[2];
+    uint64_t o_full[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kStages = (D == 128) ? 2 : 4;
+    static constexpr int kChunks = D / 64;                 // 64-column (128-byte) swizzle chunks
+    static constexpr uint32_t kChunkQ = BM * 128;          // bytes of one chunk of a Q tile
+    static constexpr uint32_t kChunkKV = BN * 128;
+    static constexpr uint32_t kQBytes = BM * D * 2;
+    static constexpr uint32_t kKVBytes = BN * D * 2;
+    static constexpr uint32_t kOffQ = 0;
+    static constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;
+    static constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
+    static constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
+    static constexpr uint32_t kSmemBytes = kOffBar + sizeof(FwdBarriers) + 1024;  // + alignment slack
+    __host__ __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 128; }
+    __host__ __device__ static constexpr uint32_t col_o(int t) { return 256 + (uint32_t)t * D; }
+    static constexpr uint32_t kTmemCols = 512;
+};
+
+// Waits that run out of budget, or see another warp's abort, make the whole warp stop.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    bool ok = mbar_wait(bar, parity, abort_flag);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Waits with a fixed budget and no abort check: used to drain copies in flight before exit.
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_test(bar, parity) && clock64() - t0 < kWaitBudgetCycles) {
+    }
+}
+
+template <int D>
+__device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint8_t* smem,
+                         FwdBarriers* bars, int head, int q0, int T) {
+    using C = FwdCfg<D>;
+    volatile int* abort_flag = &bars->abort;
+    const uint64_t pol_kv = policy_evict_last();
+    const uint64_t pol_q = policy_evict_first();
+    for (int t = 0; t < 2; ++t) {
+        mbar_expect_tx(&bars->q_full[t], C::kQBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffQ + t * C::kQBytes + c * C::kChunkQ, tm_q, &bars->q_full[t], c * 64,
+                        q0 + t * BM, head, pol_q);
+    }
+    int issued = 0;
+    for (int j = 0; j < T; ++j) {
+        const int s = j % C::kStages;
+        if (j >= C::kStages && !mbar_wait(&bars->kv_empty[s], ((j / C::kStages) - 1) & 1, abort_flag)) break;
+        mbar_expect_tx(&bars->k_full[s], C::kKVBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffK + s * C::kKVBytes + c * C::kChunkKV, tm_k, &bars->k_full[s], c * 64, j * BN,
+                        head, pol_kv);
+        mbar_expect_tx(&bars->v_full[s], C::kKVBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffV + s * C::kKVBytes + c * C::kChunkKV, tm_v, &bars->v_full[s], c * 64, j * BN,
+                        head, pol_kv);
+        issued = j + 1;
+    }
+    // Every load issued must have landed before the CTA may exit (only matters after an abort).
+    drain_wait(&bars->q_full[0], 0);
+    drain_wait(&bars->q_full[1], 0);
+    for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j) {
+        drain_wait(&bars->k_full[j % C::kStages], (j / C::kStages) & 1);
+        drain_wait(&bars->v_full[j % C::kStages], (j / C::kStages) & 1);
+    }
+}
+
+template <int D>
+__device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int T) {
+    using C = FwdCfg<D>;
+    volatile int* abort_flag = &bars->abort;
+    constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
+    constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);
+    const uint32_t sQ = smem_u32(smem + C::kOffQ);
+    const uint32_t sK = smem_u32(smem + C::kOffK);
+    const uint32_t sV = smem_u32(smem + C::kOffV);
+
+    auto issue_s = [&](int t, int s) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk / 4) * C::kChunkQ + (kk % 4) * 32;
+            const uint64_t a = sdesc_sw128(sQ + t * C::kQBytes + koff, 16, 1024);
+            const uint64_t b = sdesc_sw128(sK + s * C::kKVBytes + (kk / 4) * C::kChunkKV + (kk % 4) * 32, 16, 1024);
+            mma_ss(tmem + C::col_s(t), a, b, idS, kk > 0);
+        }
+    };
+    auto issue_pv = [&](int t, int s, bool accumulate) {
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+            const uint64_t b = sdesc_sw128(sV + s * C::kKVBytes + kk * 16 * 128, C::kChunkKV, 1024);
+            mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, b, idPV, (accumulate || kk > 0) ? 1u : 0u);
+        }
+    };
+
+    bool ok = mbar_wait(&bars->q_full[0], 0, abort_flag) && mbar_wait(&bars->q_full[1], 0, abort_flag);
+    for (int j = 0; ok && j < T; ++j) {
+        const int s = j % C::kStages;
+        const uint32_t ph = (j / C::kStages) & 1;
+        if (j == 0) {
+            if (!(ok = mbar_wait(&bars->k_full[s], ph, abort_flag))) break;
+            tc_fence_after();
+            issue_s(0, s);
+            mma_commit(&bars->s_full[0]);
+            issue_s(1, s);
+            mma_commit(&bars->s_full[1]);
+        }
+        const int s2 = (j + 1) % C::kStages;
+        const uint32_t ph2 = ((j + 1) / C::kStages) & 1;
+        if (!(ok = mbar_wait(&bars->v_full[s], ph, abort_flag))) break;
+        if (!(ok = mbar_wait(&bars->p_full[0], j & 1, abort_flag))) break;
+        tc_fence_after();
+        issue_pv(0, s, j > 0);
+        if (j == T - 1) mma_commit(&bars->o_full[0]);
+        if (j + 1 < T) {
+            if (!(ok = mbar_wait(&bars->k_full[s2], ph2, abort_flag))) break;
+            tc_fence_after();
+            issue_s(0, s2);
+            mma_commit(&bars->s_full[0]);
+        }
+        if (!(ok = mbar_wait(&bars->p_full[1], j & 1, abort_flag))) break;
+        tc_fence_after();
+        issue_pv(1, s, j > 0);
+        mma_commit(&bars->kv_empty[s]);
+        if (j == T - 1) mma_commit(&bars->o_full[1]);
+        if (j + 1 < T) {
+            issue_s(1, s2);
+            mma_commit(&bars->s_full[1]);
+        }
+    }
+    // Tensor memory is freed after this: every MMA issued must have completed.
+    mma_commit(&bars->mma_done);
+    drain_wait(&bars->mma_done, 0);
+}
+
+template <int D>
+__device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat16* __restrict__ o,
+                           float* __restrict__ lse, int head, int q0, int N, int T, float scale_log2) {
+    using C = FwdCfg<D>;
+    volatile int* abort_flag = &bars->abort;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int quarter = warp & 3;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + C::col_s(t) + lane_off;
+    const uint32_t tO = tmem + C::col_o(t) + lane_off;
+    const int tail = N - (T - 1) * BN;  // valid keys in the last block (1..BN)
+
+    float m_run = -INFINITY, l_run = 0.f;
+    bool ok = true;
+    for (int j = 0; j < T; ++j) {
+        if (!(ok = warp_wait(&bars->s_full[t], j & 1, abort_flag))) break;
+        tc_fence_after();
+        uint32_t r[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, r[q]);
+        tmem_ld_wait();
+        if (j == T - 1 && tail < BN) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int c = 0; c < 32; ++c)
+                    if (q * 32 + c >= tail) r[q][c] = __float_as_uint(-INFINITY);
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(r[q][c]));
+        const float m_new = fmaxf(m_run, mx * scale_log2);
+        const bool rescale = m_new - m_run > kRescaleThreshold;  // always true for the first block
+        float alpha = 1.f;
+        if (rescale) {
+            alpha = ex2(m_run - m_new);
+            m_run = m_new;
+        }
+        const float neg_m = -m_run;
+        float sum = 0.f;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                const float p0 = ex2(fmaf(__uint_as_float(r[2 * h + c / 16][(2 * c) % 32]), scale_log2, neg_m));
+                const float p1 = ex2(fmaf(__uint_as_float(r[2 * h + c / 16][(2 * c + 1) % 32]), scale_log2, neg_m));
+                sum += p0 + p1;
+                pk[c] = pack_bf16(p0, p1);
+            }
+            tmem_st32(tS + h * 32, pk);
+        }
+        l_run = l_run * alpha + sum;
+        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+            for (int q = 0; q < D / 32; ++q) {
+                uint32_t x[32];
+                tmem_ld32(tO + q * 32, x);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * alpha);
+                tmem_st32(tO + q * 32, x);
+            }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_full[t]);
+    }
+    if (!ok) return;
+    if (!warp_wait(&bars->o_full[t], 0, abort_flag)) return;
+    tc_fence_after();
+
+    const int row = q0 + t * BM + quarter * 32 + lane;
+    const float inv_l = 1.f / l_run;
+    const size_t base = ((size_t)head * N + row) * D;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t x[32];
+        tmem_ld32(tO + q * 32, x);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16(__uint_as_float(x[2 * c]) * inv_l, __uint_as_float(x[2 * c + 1]) * inv_l);
+        if (row < N) {
+            uint4* dst = reinterpret_cast<uint4*>(o + base + q * 32);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+    }
+    if (row < N) lse[(size_t)head * N + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+              int N, float scale_log2) {
+    using C = FwdCfg<D>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    FwdBarriers* bars = reinterpret_cast<FwdBarriers*>(smem + C::kOffBar);
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int head = blockIdx.y;
+    const int q0 = blockIdx.x * 2 * BM;
+    const int T = (N + BN - 1) / BN;
+
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bars->q_full[t], 1);
+            mbar_init(&bars->s_full[t], 1);
+            mbar_init(&bars->p_full[t], BM);
+            mbar_init(&bars->o_full[t], 1);
+        }
+        for (int s = 0; s < kMaxStages; ++s) {
+            mbar_init(&bars->k_full[s], 1);
+            mbar_init(&bars->v_full[s], 1);
+            mbar_init(&bars->kv_empty[s], 1);
+        }
+        mbar_init(&bars->mma_done, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == kTmaWarp && lane == 0) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+    }
+    if (warp == kMmaWarp) {
+        tmem_alloc(&bars->tmem_base, C::kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, smem, bars, head, q0, T);
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) mma_issuer<D>(smem, bars, tmem, T);
+    } else {
+        softmax_wg<D>(bars, tmem, warp / 4, o, lse, head, q0, N, T, scale_log2);
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kMmaWarp) {
+        tc_fence_after();
+        tmem_dealloc(tmem, C::kTmemCols);
+    }
+    if (threadIdx.x == 0 && bars->abort) atomicCAS(&g_fwd_status, 0, (int)FA_ERR_TIMEOUT);
+}
+
+template <int D>
+cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& s, float scale,
+                   cudaStream_t st) {
+    using C = FwdCfg<D>;
+    CUtensorMap tq, tk, tv;
+    cudaError_t e;
+    if ((e = make_tmap_bf16_3d(&tq, q, s.d, s.N, s.heads(), BM)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16_3d(&tk, k, s.d, s.N, s.heads(), BN)) != cudaSuccess) return e;
+    if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BN)) != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    dim3 grid((s.N + 2 * BM - 1) / (2 * BM), (unsigned)s.heads());
+    const float scale_log2 = scale * 1.4426950408889634f;
+    fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, s.N, scale_log2);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& s,
+                          float scale, cudaStream_t st) {
+    return s.d == 128 ? launch<128>(q, k, v, o, lse, s, scale, st) : launch<64>(q, k, v, o, lse, s, scale, st);
+}
+
+int fwd_tc_read_and_clear_status(cudaStream_t st) {
+    int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbolAsync(&v, g_fwd_status, sizeof(int), 0, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+        return -1;
+    if (cudaMemcpyToSymbolAsync(g_fwd_status, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, st) != cudaSuccess)
+        return -1;
+    if (cudaStreamSynchronize(st) != cudaSuccess) return -1;
+    return v;
+}
+
+}  // namespace fa

@@ -1,0 +1,49 @@
+// Host-side declarations shared by the translation units of libfa.so (no device code here).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/fa.h"
+
+namespace fa {
+
+// Shape of one attention call: B*H independent heads of N rows and head size d.
+struct Shape {
+    int B, H, N, d;
+    int64_t heads() const { return (int64_t)B * H; }
+    int64_t rows() const { return heads() * N; }
+};
+
+// Records a message for fa_last_error_string() and returns `st`.
+fa_status set_error(fa_status st, const char* fmt, ...);
+
+// Each kernel translation unit owns one device status word; these read it (after a stream sync)
+// and clear it.  They return the first nonzero code recorded, or 0.
+int fwd_tc_read_and_clear_status(cudaStream_t s);
+int bwd_tc_read_and_clear_status(cudaStream_t s);
+
+// Workspace sections of the backward pass (byte offsets from the workspace base).
+struct BwdWorkspace {
+    size_t dq_acc, row_d, lse2, total;
+};
+BwdWorkspace bwd_workspace_layout(const Shape& s);
+
+// Encodes a TMA descriptor for a bf16 [heads, N, d] array (d innermost) with boxes of 64 columns x
+// `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.
+cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows);
+
+// Launchers (return cudaGetLastError() of their launches).
+cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& s,
+                          float scale, cudaStream_t st);
+cudaError_t launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                                const Shape& s, float scale, cudaStream_t st);
+cudaError_t launch_fwd_simt_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
+                                 const Shape& s, float scale, cudaStream_t st);
+cudaError_t launch_bwd_simt_bf16(const void* q, const void* k, const void* v, const void* o,
+                                 const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                                 const Shape& s, float scale, float* row_d, cudaStream_t st);
+
+}  // namespace fa

@@ -1,0 +1,108 @@
+/*
+ * fa.h — C ABI of libfa.so: exact scaled dot-product attention, forward and backward, on one
+ * NVIDIA GB300 (sm_103a), computed tile by tile without ever storing the N x N score matrix.
+ *
+ * The operation.  For every batch b and head h independently,
+ *     O = softmax(scale * Q K^T) V,        LSE_i = log(sum_j exp(scale * q_i . k_j))   (natural log)
+ * which is Attention(Q,K,V) = softmax(QK^T / sqrt(d_k)) V of the FlashAttention fable on
+ * ckw19810413.github.io (section 概念揭曉), computed the way "账房先生的奔命：Flash Attention 与内存
+ * I/O 革命" §六 describes (Tiling + Online Softmax: Q cut into row blocks, K and V streamed in blocks,
+ * a running max, a running exp-sum and an output accumulator rescaled by exp(m_old - m_new)), writing
+ * only O and the softmax statistic back to device memory (that page's §六 closing remark; the
+ * 技术解读 section of "算珠楼的掌簿人").  LSE is the single statistic saved for the backward pass,
+ * which recomputes P from it instead of storing P (the same page's §七 重计算).
+ *
+ * Conventions shared by every entry point:
+ *   - Layout: q, k, v, o, dout, dq, dk, dv are contiguous row-major [B, H, N, d] arrays; lse is a
+ *     contiguous [B, H, N] fp32 array.  All pointers are DEVICE pointers, 16-byte aligned.
+ *   - Ownership: the caller allocates and frees every buffer (including the backward workspace).
+ *     The library allocates no device memory of its own and never anything of N x N size.
+ *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
+ *     call is asynchronous on that stream; results are valid once the stream has completed.  No call
+ *     synchronises the device.
+ *   - Scale: applied to the scores; 1/sqrt(d) gives the pages' definition.  Must be finite and > 0.
+ *   - No mask, no dropout, no causal option (the pages define none).
+ *   - Errors: arguments are checked on the host before anything is launched.  On FA_ERR_INVALID_ARG or
+ *     FA_ERR_UNSUPPORTED nothing was launched and no output was written.  FA_ERR_CUDA means a CUDA call
+ *     failed (the launch may have been partial).  fa_last_error_string() gives the message of the last
+ *     failing call made on the calling thread.
+ *   - Device-side waits in the kernels are bounded.  A wait that runs out of its budget stops the
+ *     kernel and records FA_ERR_TIMEOUT in a device status word, read by fa_check_status().
+ */
+#ifndef FA_H_
+#define FA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, B/H/N < 1, bad scale, workspace too small */
+    FA_ERR_UNSUPPORTED = 2,   /* a head size or shape this build has no kernel for */
+    FA_ERR_CUDA = 3,          /* a CUDA runtime/driver call or a launch failed */
+    FA_ERR_TIMEOUT = 4        /* a bounded device-side wait expired (reported by fa_check_status) */
+} fa_status;
+
+/*
+ * fa_fwd — bf16 forward on the tensor cores (tcgen05, fp32 accumulation in tensor memory).
+ *   q, k, v : const bf16 [B,H,N,d]        (inputs)
+ *   o       : bf16 [B,H,N,d]              (output, O = softmax(scale Q K^T) V rounded to bf16)
+ *   lse     : float [B,H,N]               (output, natural-log log-sum-exp of each scaled score row)
+ *   d       : 64 or 128 (FA_ERR_UNSUPPORTED otherwise).  N may be any value >= 1 (ragged tails are masked).
+ *   Product B*H must fit in 2^31 - 1; N*d in 2^31 - 1.
+ */
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, void* stream);
+
+/*
+ * fa_fwd_f32 — fp32 forward on the CUDA cores (no tensor-core rounding of any operand).
+ *   q, k, v, o : float [B,H,N,d];  lse : float [B,H,N].
+ *   d          : 1 .. 128 and a multiple of 4 (FA_ERR_UNSUPPORTED otherwise).
+ *   Same tiled, online-softmax method as fa_fwd, for callers that need fp32 results.
+ */
+fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,
+                     int B, int H, int N, int d, float scale, void* stream);
+
+/*
+ * fa_bwd_workspace_size — bytes of device scratch fa_bwd needs for this shape: an fp32 dQ accumulator
+ * [B,H,N,d] and two fp32 per-row arrays [B,H,N] (the row term D_i = dO_i . O_i and the log2-domain
+ * LSE), each section rounded up to 256 bytes.  Returns 0 for invalid shapes.
+ */
+size_t fa_bwd_workspace_size(int B, int H, int N, int d);
+
+/*
+ * fa_bwd — bf16 backward: gradients of O(Q,K,V) contracted with dout.
+ *   q, k, v    : const bf16 [B,H,N,d]  (the forward's inputs)
+ *   o          : const bf16 [B,H,N,d]  (the forward's output)
+ *   dout       : const bf16 [B,H,N,d]  (upstream gradient dO)
+ *   lse        : const float [B,H,N]   (the forward's LSE output)
+ *   dq, dk, dv : bf16 [B,H,N,d]        (outputs)
+ *   workspace  : device scratch of at least fa_bwd_workspace_size(B,H,N,d) bytes, 256-byte aligned;
+ *                its contents on entry do not matter and are overwritten.
+ *   d          : 64 or 128.
+ * P is recomputed tile by tile from q, k and lse (it is never stored); dV = P^T dO, dP = dO V^T,
+ * dS = P o (dP - D), dK = scale dS^T Q, dQ = scale dS K with D_i = dO_i . O_i.
+ */
+fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                 const float* lse, void* dq, void* dk, void* dv,
+                 int B, int H, int N, int d, float scale,
+                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* Message of the last failing call on the calling thread ("" if none).  Valid until the next call. */
+const char* fa_last_error_string(void);
+
+/*
+ * fa_check_status — synchronises `stream`, then reports and clears the device status word:
+ * FA_ERR_TIMEOUT if a kernel gave up a bounded wait since the last check, FA_ERR_CUDA if the stream
+ * reported an error, else FA_OK.  A debugging and test helper; the fast path never calls it.
+ */
+fa_status fa_check_status(void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FA_H_ */

@@ -1,0 +1,111 @@
+"""GPU backward parity: dQ, dK, dV of the CUDA path against the fp64 oracle (relative Frobenius error)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import fa_inputs
+import oracle
+from parity_util import TOL_GRAD_BF16, need_gpu, np64, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_fwd_bwd(fa, inp, scale):
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fa_fwd(q, k, v, scale)
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, do, lse, scale)
+    torch.cuda.synchronize()
+    fa.fa_check_status()
+    return o, lse, dq, dk, dv
+
+
+def _check_full(fa, B, H, N, d, seed, q_gain=1.0):
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed, q_gain, with_grad=True)
+    scale = 1 / math.sqrt(d)
+    _, _, dq, dk, dv = _gpu_fwd_bwd(fa, inp, scale)
+    rq, rk, rv = oracle.backward(*(np64(inp[n]) for n in ("q", "k", "v", "do")), scale)
+    errs = rel_fro(np64(dq), rq), rel_fro(np64(dk), rk), rel_fro(np64(dv), rv)
+    assert max(errs) <= TOL_GRAD_BF16, (B, H, N, d, errs)
+    return errs
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 7, 64, 65, 128, 129, 200, 383, 512])
+def test_bwd_ragged(N, d):
+    fa = need_gpu()
+    _check_full(fa, 1, 2, N, d, seed=800 + N + d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_several_heads(d):
+    fa = need_gpu()
+    _check_full(fa, 2, 3, 1000, d, seed=900 + d)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_bwd_peaky_rows(d):
+    fa = need_gpu()
+    _check_full(fa, 1, 2, 777, d, seed=950 + d, q_gain=4.0)
+
+
+def test_bwd_gradient_invariants_on_gpu_outputs():
+    """sum_j dK_j = 0 and sum_j dV_j = sum_i dO_i hold for exact gradients at any size."""
+    fa = need_gpu()
+    B, H, N, d = 1, 4, 3000, 128
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", 990, with_grad=True)
+    _, _, dq, dk, dv = _gpu_fwd_bwd(fa, inp, 1 / math.sqrt(d))
+    dk_sum = dk.double().sum(dim=2)
+    dv_sum = dv.double().sum(dim=2)
+    do_sum = inp["do"].double().sum(dim=2).cuda()
+    scale_k = dk.double().abs().sum(dim=2)
+    assert (dk_sum.abs() <= 2e-2 * scale_k + 1e-3).all()
+    assert ((dv_sum - do_sum).abs() <= 2e-2 * dv.double().abs().sum(dim=2) + 1e-3).all()
+
+
+def test_workload_b4_h16_n2048_d64_full():
+    fa = need_gpu()
+    w = fa_inputs.WORKLOADS["bf16-fwdbwd-B4-H16-N2048-d64"]
+    inp = fa_inputs.workload_inputs(w)
+    _, _, dq, dk, dv = _gpu_fwd_bwd(fa, inp, w.scale)
+    rq, rk, rv = oracle.backward(*(np64(inp[n]) for n in ("q", "k", "v", "do")), w.scale)
+    errs = rel_fro(np64(dq), rq), rel_fro(np64(dk), rk), rel_fro(np64(dv), rv)
+    assert max(errs) <= TOL_GRAD_BF16, errs
+
+
+def test_workload_b1_h16_n8192_d128_sampled():
+    """Full-size launch; the oracle checks 256 query rows (dQ) and 256 key rows (dK, dV) of two heads."""
+    fa = need_gpu()
+    w = fa_inputs.WORKLOADS["bf16-fwdbwd-B1-H16-N8192-d128"]
+    inp = fa_inputs.workload_inputs(w)
+    _, _, dq, dk, dv = _gpu_fwd_bwd(fa, inp, w.scale)
+    heads = [0, 11]
+    qrows = fa_inputs.sample_rows(w.N, w.H, 256, seed_base=1000)
+    krows = fa_inputs.sample_rows(w.N, w.H, 256, seed_base=2000)
+    sub = {n: np64(inp[n][:, heads]) for n in ("q", "k", "v", "do")}
+    rq, rk, rv = oracle.backward_rows(sub["q"], sub["k"], sub["v"], sub["do"], w.scale,
+                                      [qrows[h].numpy() for h in heads], [krows[h].numpy() for h in heads])
+    gq = np.stack([np64(dq[:, h, qrows[h]]) for h in heads], axis=1)
+    gk = np.stack([np64(dk[:, h, krows[h]]) for h in heads], axis=1)
+    gv = np.stack([np64(dv[:, h, krows[h]]) for h in heads], axis=1)
+    errs = rel_fro(gq, rq), rel_fro(gk, rk), rel_fro(gv, rv)
+    assert max(errs) <= TOL_GRAD_BF16, errs
+    for t in (dq, dk, dv):
+        assert torch.isfinite(t.float()).all()
+
+
+def test_bwd_workspace_contents_do_not_matter():
+    fa = need_gpu()
+    B, H, N, d = 1, 2, 300, 64
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", 991, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fa_fwd(q, k, v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    ws.fill_(0x7f)
+    g1 = fa.fa_bwd(q, k, v, o, do, lse, workspace=ws)
+    ws.fill_(0xff)
+    g2 = fa.fa_bwd(q, k, v, o, do, lse, workspace=ws)
+    torch.cuda.synchronize()
+    for a, b in zip(g1, g2):
+        assert rel_fro(np64(a), np64(b)) <= 1e-2
