@@ -19,7 +19,11 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = ran
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA", 4: "FA_ERR_TIMEOUT"}
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_last_error_string", "fa_check_status")
+EXPORTS = ("fa_fwd", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc", "fa_last_error_string",
+           "fa_check_status")
+
+# Bytes of the static scratch that fa_bwd_noalloc uses (FA_BWD_NOALLOC_MAX_SCRATCH_BYTES).
+NOALLOC_MAX_SCRATCH_BYTES = 32 << 20
 
 _lib = None
 
@@ -47,6 +51,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_bwd_workspace_size.restype = Z
     lib.fa_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P, Z, P]
     lib.fa_bwd.restype = I
+    lib.fa_bwd_noalloc.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, F, P]
+    lib.fa_bwd_noalloc.restype = I
     lib.fa_last_error_string.argtypes = []
     lib.fa_last_error_string.restype = ctypes.c_char_p
     lib.fa_check_status.argtypes = [P]
@@ -136,6 +142,23 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, dq=None, dk=None, dv=None, workspace
     return dq, dk, dv
 
 
+def fa_bwd_noalloc(q, k, v, o, do, lse, scale=None, dq=None, dk=None, dv=None, stream=None):
+    """bf16 backward that allocates no scratch: the library's static scratch array stands in for the
+    workspace (for callers that cannot allocate device memory).  Pass preallocated dq, dk, dv to make
+    the call allocate nothing at all; shapes needing more than NOALLOC_MAX_SCRATCH_BYTES of scratch
+    raise FAError (FA_ERR_INVALID_ARG)."""
+    B, H, N, d = _shape(q)
+    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
+        _check_tensor(name, t, (B, H, N, d), torch.bfloat16)
+    _check_tensor("lse", lse, (B, H, N), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check(load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                         _ptr(dk), _ptr(dv), B, H, N, d, _default_scale(d, scale), _stream(stream)))
+    return dq, dk, dv
+
+
 def fa_check_status(stream=None):
     _check(load_library().fa_check_status(_stream(stream)))
 
@@ -144,5 +167,6 @@ def fa_last_error_string() -> str:
     return load_library().fa_last_error_string().decode(errors="replace")
 
 
-__all__ = ["fa_fwd", "fa_fwd_f32", "fa_bwd", "fa_bwd_workspace_size", "fa_check_status", "fa_last_error_string",
+__all__ = ["fa_fwd", "fa_fwd_f32", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc", "fa_check_status",
+           "fa_last_error_string",
            "load_library", "FAError", "EXPORTS", "LIB_PATH"]

@@ -16,7 +16,8 @@
  *   - Layout: q, k, v, o, dout, dq, dk, dv are contiguous row-major [B, H, N, d] arrays; lse is a
  *     contiguous [B, H, N] fp32 array.  All pointers are DEVICE pointers, 16-byte aligned.
  *   - Ownership: the caller allocates and frees every buffer (including the backward workspace).
- *     The library allocates no device memory of its own and never anything of N x N size.
+ *     The library allocates no device memory of its own (its one fixed device array is the scratch of
+ *     fa_bwd_noalloc) and never anything of N x N size.
  *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
  *     call is asynchronous on that stream; results are valid once the stream has completed.  No call
  *     synchronises the device.
@@ -90,6 +91,28 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const float* lse, void* dq, void* dk, void* dv,
                  int B, int H, int N, int d, float scale,
                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * fa_bwd_noalloc — fa_bwd for callers that cannot allocate device memory.  The pages have no
+ * counterpart to this call; it exists for callers that receive only their input and output buffers
+ * (for example an operator plugin whose host framework owns all device memory) or that must not call
+ * cudaMalloc because it can synchronise the device.
+ *   Arguments: as fa_bwd, without the workspace.  The call allocates nothing: it uses a scratch array
+ *   of FA_BWD_NOALLOC_MAX_SCRATCH_BYTES (32 MiB) compiled into the library, which every GPU that loads
+ *   the library holds until the process exits.
+ *   Limit: shapes with fa_bwd_workspace_size(B,H,N,d) > FA_BWD_NOALLOC_MAX_SCRATCH_BYTES are rejected
+ *   with FA_ERR_INVALID_ARG before anything is launched (for d = 128: B*H*N above about 64 thousand rows).
+ *   Set-up: the first call on a device (made with that device current, like every call) looks up the
+ *   array's device address with cudaGetSymbolAddress; make that first call before any stream capture.
+ *   Sharing: all calls on a device share the one array, which keeps the last call's contents (the
+ *   kernels clear whatever must start at zero).  Calls whose executions overlap on the GPU (on
+ *   different streams, or from different threads) race on the array and give wrong results: order
+ *   them on one stream or with events.
+ */
+#define FA_BWD_NOALLOC_MAX_SCRATCH_BYTES (32u << 20)
+fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv,
+                         int B, int H, int N, int d, float scale, void* stream);
 
 /* Message of the last failing call on the calling thread ("" if none).  Valid until the next call. */
 const char* fa_last_error_string(void);
