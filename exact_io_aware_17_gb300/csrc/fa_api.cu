@@ -25,10 +25,11 @@ static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 BwdWorkspace bwd_workspace_layout(const Shape& s) {
     BwdWorkspace w;
     const size_t rows = (size_t)s.rows();
+    const size_t padded = (size_t)s.heads() * bwd_padded_rows(s.N);
     w.dq_acc = 0;
     w.row_d = round256(rows * (size_t)s.d * sizeof(float));
-    w.lse2 = w.row_d + round256(rows * sizeof(float));
-    w.total = w.lse2 + round256(rows * sizeof(float));
+    w.lse2 = w.row_d + round256(padded * sizeof(float));
+    w.total = w.lse2 + round256(padded * sizeof(float));
     return w;
 }
 
@@ -134,9 +135,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
     BwdWorkspace w = bwd_workspace_layout(s);
     if (workspace_bytes < w.total)
         return set_error(FA_ERR_INVALID_ARG, "fa_bwd: workspace holds %zu bytes, needs %zu", workspace_bytes, w.total);
-    char* ws = (char*)workspace;
-    return launch_result("fa_bwd", launch_bwd_simt_bf16(q, k, v, o, dout, lse, dq, dk, dv, s, scale,
-                                                         (float*)(ws + w.row_d), (cudaStream_t)stream));
+    return launch_result("fa_bwd", launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, s, scale, workspace,
+                                                 (cudaStream_t)stream));
 }
 
 fa_status fa_check_status(void* stream) {

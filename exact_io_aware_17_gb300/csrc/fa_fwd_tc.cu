@@ -73,19 +73,6 @@ struct FwdCfg {
     static constexpr uint32_t kTmemCols = 512;
 };
 
-// Waits that run out of budget, or see another warp's abort, make the whole warp stop.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    bool ok = mbar_wait(bar, parity, abort_flag);
-    return __all_sync(0xffffffffu, ok);
-}
-
-// Waits with a fixed budget and no abort check: used to drain copies in flight before exit.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
-    const long long t0 = clock64();
-    while (!mbar_test(bar, parity) && clock64() - t0 < kWaitBudgetCycles) {
-    }
-}
-
 template <int D>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint8_t* smem,
                          FwdBarriers* bars, int head, int q0, int T) {

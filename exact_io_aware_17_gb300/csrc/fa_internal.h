@@ -30,6 +30,8 @@ struct BwdWorkspace {
     size_t dq_acc, row_d, lse2, total;
 };
 BwdWorkspace bwd_workspace_layout(const Shape& s);
+// Rows per head of the backward's per-row arrays: N rounded up to the 64-query block of the kernel.
+inline int bwd_padded_rows(int N) { return (N + 63) / 64 * 64; }
 
 // Encodes a TMA descriptor for a bf16 [heads, N, d] array (d innermost) with boxes of 64 columns x
 // `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.
@@ -40,10 +42,8 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, 
                           float scale, cudaStream_t st);
 cudaError_t launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                                 const Shape& s, float scale, cudaStream_t st);
-cudaError_t launch_fwd_simt_bf16(const void* q, const void* k, const void* v, void* o, float* lse,
-                                 const Shape& s, float scale, cudaStream_t st);
-cudaError_t launch_bwd_simt_bf16(const void* q, const void* k, const void* v, const void* o,
-                                 const void* dout, const float* lse, void* dq, void* dk, void* dv,
-                                 const Shape& s, float scale, float* row_d, cudaStream_t st);
+cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                          const float* lse, void* dq, void* dk, void* dv, const Shape& s, float scale,
+                          void* workspace, cudaStream_t st);
 
 }  // namespace fa
