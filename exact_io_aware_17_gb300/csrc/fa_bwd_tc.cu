@@ -136,45 +136,47 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
     constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, 0, 0);   // S^T, dP^T: A K-major [keys][d], B K-major [q][d]
     constexpr uint32_t idG = idesc_bf16_f32(BK, D, 0, 1);    // dV, dK: A from TMEM, B MN-major [q][d]
     constexpr uint32_t idQ = idesc_bf16_f32(128, BQ, 1, 1);  // dQ^T: A = K^T (MN-major), B = dS^T (MN-major)
-    const uint32_t sK = smem_u32(smem + C::kOffK);
-    const uint32_t sV = smem_u32(smem + C::kOffV);
-    const uint32_t sQ = smem_u32(smem + C::kOffQ);
-    const uint32_t sDO = smem_u32(smem + C::kOffDO);
-    const uint32_t sDS = smem_u32(smem + C::kOffDS);
+    // Operand descriptors are built once; each use only adds a constant byte offset.  K-major views
+    // serve S^T and dP^T; MN-major views of the same tiles serve dV, dK and dQ^T.
+    const uint64_t kK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    const uint64_t kV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
+    const uint64_t kQ = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t kDO = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
+    const uint64_t mQ = sdesc_sw128(smem_u32(smem + C::kOffQ), C::kChunkQ, 1024);
+    const uint64_t mDO = sdesc_sw128(smem_u32(smem + C::kOffDO), C::kChunkQ, 1024);
+    const uint64_t mK = sdesc_sw128(smem_u32(smem + C::kOffK), C::kChunkK, 1024);
+    const uint64_t mDS = sdesc_sw128(smem_u32(smem + C::kOffDS), C::kDSBytes, 1024);
 
     // X^T = A_tile B_tile^T with both tiles K-major over the head dimension (S^T or dP^T).
-    auto qk_like = [&](uint32_t a_tile, uint32_t b_tile, uint32_t dst) {
+    auto qk_like = [&](uint64_t a0, uint64_t b0, uint32_t dst) {
+        const uint32_t d = tmem + dst;
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(a_tile + (kk / 4) * C::kChunkK + (kk % 4) * 32, 16, 1024);
-            const uint64_t b = sdesc_sw128(b_tile + (kk / 4) * C::kChunkQ + (kk % 4) * 32, 16, 1024);
-            mma_ss(tmem + dst, a, b, idS, kk > 0);
-        }
+        for (int kk = 0; kk < D / 16; ++kk)
+            mma_ss(d, sdesc_advance(a0, (kk / 4) * C::kChunkK + (kk % 4) * 32),
+                   sdesc_advance(b0, (kk / 4) * C::kChunkQ + (kk % 4) * 32), idS, kk > 0);
     };
     // G += A[tmem] B_tile with B MN-major over the query block (dV or dK).
-    auto grad = [&](uint32_t a_col, uint32_t b_tile, uint32_t dst, bool acc) {
+    auto grad = [&](uint32_t a_col, uint64_t b0, uint32_t dst, bool acc) {
+        const uint32_t d = tmem + dst, a = tmem + a_col;
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk) {
-            const uint64_t b = sdesc_sw128(b_tile + kk * 16 * 128, C::kChunkQ, 1024);
-            mma_ts(tmem + dst, tmem + a_col + kk * 8, b, idG, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BQ / 16; ++kk)
+            mma_ts(d, a + kk * 8, sdesc_advance(b0, kk * 16 * 128), idG, (acc || kk > 0) ? 1u : 0u);
     };
     // dQ^T = K^T dS^T over the 128 keys.
     auto dq = [&](int buf) {
+        const uint32_t d = tmem + C::kColDQ;
+        const uint64_t b0 = sdesc_advance(mDS, buf * C::kDSBytes);
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t a = sdesc_sw128(sK + kk * 16 * 128, C::kChunkK, 1024);
-            const uint64_t b = sdesc_sw128(sDS + buf * C::kDSBytes + kk * 16 * 128, C::kDSBytes, 1024);
-            mma_ss(tmem + C::kColDQ, a, b, idQ, kk > 0);
-        }
+        for (int kk = 0; kk < BK / 16; ++kk)
+            mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(b0, kk * 16 * 128), idQ, kk > 0);
     };
 
     bool ok = mbar_wait(&bars->kv_full, 0, abort_flag) && mbar_wait(&bars->qdo_full[0], 0, abort_flag);
     if (ok) {
         tc_fence_after();
-        qk_like(sK, sQ, C::col_s(0));
+        qk_like(kK, kQ, C::col_s(0));
         mma_commit(&bars->s_full[0]);
-        qk_like(sV, sDO, C::kColDP);
+        qk_like(kV, kDO, C::kColDP);
         mma_commit(&bars->dp_full);
     }
     for (int i = 0; ok && i < Tq; ++i) {
@@ -184,15 +186,15 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         if (i + 1 < Tq) {
             if (!(ok = mbar_wait(&bars->qdo_full[s1], ((i + 1) / kStages) & 1, abort_flag))) break;
             tc_fence_after();
-            qk_like(sK, sQ + s1 * C::kQBytes, C::col_s(buf ^ 1));
+            qk_like(kK, sdesc_advance(kQ, s1 * C::kQBytes), C::col_s(buf ^ 1));
             mma_commit(&bars->s_full[buf ^ 1]);
         }
         if (!(ok = mbar_wait(&bars->p_ready, i & 1, abort_flag))) break;
         tc_fence_after();
-        grad(C::col_s(buf), sDO + s * C::kQBytes, C::kColDV, i > 0);
+        grad(C::col_s(buf), sdesc_advance(mDO, s * C::kQBytes), C::kColDV, i > 0);
         if (!(ok = mbar_wait(&bars->ds_ready, i & 1, abort_flag))) break;
         tc_fence_after();
-        grad(C::kColDP, sQ + s * C::kQBytes, C::kColDK, i > 0);
+        grad(C::kColDP, sdesc_advance(mQ, s * C::kQBytes), C::kColDK, i > 0);
         mma_commit(&bars->qdo_empty[s]);
         if (i > 0 && !(ok = mbar_wait(&bars->dq_empty, (i - 1) & 1, abort_flag))) break;
         tc_fence_after();
@@ -200,7 +202,7 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free[buf]);
         if (i + 1 < Tq) {
-            qk_like(sV, sDO + s1 * C::kQBytes, C::kColDP);
+            qk_like(kV, sdesc_advance(kDO, s1 * C::kQBytes), C::kColDP);
             mma_commit(&bars->dp_full);
         }
     }

@@ -115,25 +115,28 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
     volatile int* abort_flag = &bars->abort;
     constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
     constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);
-    const uint32_t sQ = smem_u32(smem + C::kOffQ);
-    const uint32_t sK = smem_u32(smem + C::kOffK);
-    const uint32_t sV = smem_u32(smem + C::kOffV);
+    // Operand descriptors are built once; each k-step only adds a constant byte offset.
+    const uint64_t dQ0 = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
+    const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
+    const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::kOffV), C::kChunkKV, 1024);
 
     auto issue_s = [&](int t, int s) {
+        const uint64_t a0 = sdesc_advance(dQ0, t * C::kQBytes);
+        const uint64_t b0 = sdesc_advance(dK0, s * C::kKVBytes);
+        const uint32_t d = tmem + C::col_s(t);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk / 4) * C::kChunkQ + (kk % 4) * 32;
-            const uint64_t a = sdesc_sw128(sQ + t * C::kQBytes + koff, 16, 1024);
-            const uint64_t b = sdesc_sw128(sK + s * C::kKVBytes + (kk / 4) * C::kChunkKV + (kk % 4) * 32, 16, 1024);
-            mma_ss(tmem + C::col_s(t), a, b, idS, kk > 0);
+            mma_ss(d, sdesc_advance(a0, (kk / 4) * C::kChunkQ + (kk % 4) * 32),
+                   sdesc_advance(b0, (kk / 4) * C::kChunkKV + (kk % 4) * 32), idS, kk > 0);
         }
     };
     auto issue_pv = [&](int t, int s, bool accumulate) {
+        const uint64_t b0 = sdesc_advance(dV0, s * C::kKVBytes);
+        const uint32_t d = tmem + C::col_o(t);
+        const uint32_t a = tmem + C::col_s(t);
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-            const uint64_t b = sdesc_sw128(sV + s * C::kKVBytes + kk * 16 * 128, C::kChunkKV, 1024);
-            mma_ts(tmem + C::col_o(t), tmem + C::col_s(t) + kk * 8, b, idPV, (accumulate || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(d, a + kk * 8, sdesc_advance(b0, kk * 16 * 128), idPV, (accumulate || kk > 0) ? 1u : 0u);
     };
 
     bool ok = mbar_wait(&bars->q_full[0], 0, abort_flag) && mbar_wait(&bars->q_full[1], 0, abort_flag);

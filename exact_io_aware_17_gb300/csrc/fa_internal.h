@@ -6,7 +6,7 @@
 #include <stddef.h>
 #include <stdint.h>
 
-#include "../../include/fa.h"
+#include "fa.h"
 
 namespace fa {
 

@@ -193,6 +193,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
+// Descriptor of the same operand `bytes` further on in shared memory (bytes a multiple of 16).  The
+// start-address field holds address / 16 in 14 bits and every shared address here is below 256 KB, so
+// the add never carries out of the field.  Building a descriptor once per tile and moving it with this
+// add keeps the single MMA-issuing thread fast enough to feed the tensor core.
+__host__ __device__ constexpr uint64_t sdesc_advance(uint64_t desc, uint32_t bytes) { return desc + (bytes >> 4); }
+
 // ---------------------------------------------------------------- tcgen05: TMEM <-> registers
 // Each thread of the warp reads 32 consecutive 32-bit columns of its own lane (lane = 32*(warp%4) + laneid).
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
