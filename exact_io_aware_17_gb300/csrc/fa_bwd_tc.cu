@@ -50,7 +50,7 @@ constexpr int BQ = 64;   // queries per step
 constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 
 struct BwdBarriers {
     uint64_t kv_full;
