@@ -12,13 +12,15 @@
 //                     fp32 dQ accumulator.
 //   bwd_tc_kernel     one CTA per (head, block of 128 keys).  K_j, V_j stay in shared memory; the CTA
 //                     walks every block of 64 queries i:
-//                         S^T  = K_j Q_i^T            (tensor memory, fp32; double buffered)
+//                         S^T  = K_j Q_i^T            K_j as bf16 from tensor memory; fp32 result,
+//                                                     double buffered
 //                         dP^T = V_j dO_i^T
 //                         P^T  = exp2(S^T scale log2e - LSE2_i)    thread = key row
 //                         dS^T = P^T o (dP^T - D_i)
 //                         dV_j += P^T dO_i            P^T as bf16 from tensor memory
 //                         dK_j += dS^T Q_i            dS^T as bf16 from tensor memory
-//                         dQ_i^T = K_j^T dS^T         dS^T as bf16 from shared memory
+//                         dQ_i^T = K_j^T dS^T         dS^T as bf16 from shared memory, into the
+//                                                     S^T buffer of the step (free once dV used P^T)
 //                     and adds dQ_i into the fp32 accumulator with bulk reduce-add copies.
 //   bwd_dq_convert    dQ = bf16(scale * accumulator).
 //
@@ -29,8 +31,11 @@
 // For d = 64 the dQ^T product still uses M = 128: the A operand's second 64-row half points at a
 // zeroed shared-memory block, and the rows it produces are ignored.
 //
-// TMEM columns: S^T [0,64) and [64,128) (P^T as bf16 over the first 32 of each), dP^T [128,192)
-// (dS^T as bf16 over its first 32), dQ^T [192,256), dV [256,256+D), dK [256+D,256+2D).
+// TMEM columns: two step buffers [0,64) and [64,128), each holding S^T, then P^T as bf16 over its
+// first 32 columns, then dQ^T; dP^T [128,192) (dS^T as bf16 over its first 32); K_j as bf16 [192,192+D/2)
+// (the A operand of S^T: it stays resident, so S^T reads only Q_i from shared memory); dV [256,256+D),
+// dK [256+D,256+2D).  Shared-memory bandwidth is what bounds this kernel, so every operand that can
+// come from tensor memory does.
 
 #include <cuda_bf16.h>
 #include <math.h>
@@ -64,6 +69,7 @@ struct BwdBarriers {
     uint64_t dq_empty;
     uint64_t ds_free[2];
     uint64_t dkdv_full;
+    uint64_t ka_ready;
     uint64_t mma_done;
     uint32_t tmem_base;
     int abort;
@@ -90,7 +96,7 @@ struct BwdCfg {
     static constexpr uint32_t kOffRows = kOffDQ + kDQBytes; // [stage][2][BQ] floats
     static constexpr uint32_t kOffBar = kOffRows + kStages * 2 * kRowBytes;
     static constexpr uint32_t kSmemBytes = kOffBar + sizeof(BwdBarriers) + 1024;
-    static constexpr uint32_t kColDP = 128, kColDQ = 192, kColDV = 256, kColDK = 256 + D;
+    static constexpr uint32_t kColDP = 128, kColKA = 192, kColDV = 256, kColDK = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
     __host__ __device__ static constexpr uint32_t col_s(int b) { return (uint32_t)b * 64; }
 };
@@ -133,12 +139,11 @@ template <int D>
 __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq) {
     using C = BwdCfg<D>;
     volatile int* abort_flag = &bars->abort;
-    constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, 0, 0);   // S^T, dP^T: A K-major [keys][d], B K-major [q][d]
+    constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, 0, 0);   // S^T (A from TMEM), dP^T (A K-major); B K-major [q][d]
     constexpr uint32_t idG = idesc_bf16_f32(BK, D, 0, 1);    // dV, dK: A from TMEM, B MN-major [q][d]
     constexpr uint32_t idQ = idesc_bf16_f32(128, BQ, 1, 1);  // dQ^T: A = K^T (MN-major), B = dS^T (MN-major)
     // Operand descriptors are built once; each use only adds a constant byte offset.  K-major views
     // serve S^T and dP^T; MN-major views of the same tiles serve dV, dK and dQ^T.
-    const uint64_t kK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t kV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
     const uint64_t kQ = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
     const uint64_t kDO = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
@@ -147,7 +152,14 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
     const uint64_t mK = sdesc_sw128(smem_u32(smem + C::kOffK), C::kChunkK, 1024);
     const uint64_t mDS = sdesc_sw128(smem_u32(smem + C::kOffDS), C::kDSBytes, 1024);
 
-    // X^T = A_tile B_tile^T with both tiles K-major over the head dimension (S^T or dP^T).
+    // S^T = K Q_i^T with K from tensor memory and Q_i K-major over the head dimension.
+    auto s_mma = [&](uint64_t b0, uint32_t dst) {
+        const uint32_t d = tmem + dst, a = tmem + C::kColKA;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk)
+            mma_ts(d, a + kk * 8, sdesc_advance(b0, (kk / 4) * C::kChunkQ + (kk % 4) * 32), idS, kk > 0);
+    };
+    // dP^T = V dO_i^T with both tiles K-major over the head dimension.
     auto qk_like = [&](uint64_t a0, uint64_t b0, uint32_t dst) {
         const uint32_t d = tmem + dst;
 #pragma unroll
@@ -162,19 +174,20 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         for (int kk = 0; kk < BQ / 16; ++kk)
             mma_ts(d, a + kk * 8, sdesc_advance(b0, kk * 16 * 128), idG, (acc || kk > 0) ? 1u : 0u);
     };
-    // dQ^T = K^T dS^T over the 128 keys.
+    // dQ^T = K^T dS^T over the 128 keys, into the step's buffer.
     auto dq = [&](int buf) {
-        const uint32_t d = tmem + C::kColDQ;
+        const uint32_t d = tmem + C::col_s(buf);
         const uint64_t b0 = sdesc_advance(mDS, buf * C::kDSBytes);
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
             mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(b0, kk * 16 * 128), idQ, kk > 0);
     };
 
-    bool ok = mbar_wait(&bars->kv_full, 0, abort_flag) && mbar_wait(&bars->qdo_full[0], 0, abort_flag);
+    bool ok = mbar_wait(&bars->kv_full, 0, abort_flag) && mbar_wait(&bars->qdo_full[0], 0, abort_flag) &&
+              mbar_wait(&bars->ka_ready, 0, abort_flag);
     if (ok) {
         tc_fence_after();
-        qk_like(kK, kQ, C::col_s(0));
+        s_mma(kQ, C::col_s(0));
         mma_commit(&bars->s_full[0]);
         qk_like(kV, kDO, C::kColDP);
         mma_commit(&bars->dp_full);
@@ -185,8 +198,10 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         const int buf = i & 1;
         if (i + 1 < Tq) {
             if (!(ok = mbar_wait(&bars->qdo_full[s1], ((i + 1) / kStages) & 1, abort_flag))) break;
+            // Buffer buf^1 last held dQ^T of step i-1: it must have been drained.
+            if (i > 0 && !(ok = mbar_wait(&bars->dq_empty, (i - 1) & 1, abort_flag))) break;
             tc_fence_after();
-            qk_like(kK, sdesc_advance(kQ, s1 * C::kQBytes), C::col_s(buf ^ 1));
+            s_mma(sdesc_advance(kQ, s1 * C::kQBytes), C::col_s(buf ^ 1));
             mma_commit(&bars->s_full[buf ^ 1]);
         }
         if (!(ok = mbar_wait(&bars->p_ready, i & 1, abort_flag))) break;
@@ -196,8 +211,6 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         tc_fence_after();
         grad(C::kColDP, sdesc_advance(mQ, s * C::kQBytes), C::kColDK, i > 0);
         mma_commit(&bars->qdo_empty[s]);
-        if (i > 0 && !(ok = mbar_wait(&bars->dq_empty, (i - 1) & 1, abort_flag))) break;
-        tc_fence_after();
         dq(buf);
         mma_commit(&bars->dq_full);
         mma_commit(&bars->ds_free[buf]);
@@ -224,6 +237,26 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, __
     const bool valid_key = k0 + r < N;
     uint8_t* ds_tile = smem + C::kOffDS;
     const float* rows_base = reinterpret_cast<const float*>(smem + C::kOffRows);
+
+    // K row r into tensor memory as packed bf16 pairs: the resident A operand of S^T.
+    if (!warp_wait(&bars->kv_full, 0, abort_flag)) return;
+#pragma unroll
+    for (int c = 0; c < C::kChunks; ++c) {
+        uint32_t w[32];
+        const uint8_t* krow = smem + C::kOffK + c * C::kChunkK + r * 128;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const uint4 x = *reinterpret_cast<const uint4*>(krow + ((p ^ (r & 7)) << 4));
+            w[4 * p] = x.x;
+            w[4 * p + 1] = x.y;
+            w[4 * p + 2] = x.z;
+            w[4 * p + 3] = x.w;
+        }
+        tmem_st32(tmem + lane_off + C::kColKA + c * 32, w);
+    }
+    tmem_st_wait();
+    tc_fence_before();
+    mbar_arrive(&bars->ka_ready);
 
     bool ok = true;
     for (int i = 0; i < Tq; ++i) {
@@ -332,8 +365,8 @@ __device__ void bwd_dq_drain(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         if (!failed) {
             tc_fence_after();
             if (active) {
-                tmem_ld32(tmem + lane_off + C::kColDQ, x[0]);
-                tmem_ld32(tmem + lane_off + C::kColDQ + 32, x[1]);
+                tmem_ld32(tmem + lane_off + C::col_s(i & 1), x[0]);
+                tmem_ld32(tmem + lane_off + C::col_s(i & 1) + 32, x[1]);
                 tmem_ld_wait();
             }
             tc_fence_before();
@@ -388,6 +421,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_init(&bars->dq_full, 1);
         mbar_init(&bars->dq_empty, 128);
         mbar_init(&bars->dkdv_full, 1);
+        mbar_init(&bars->ka_ready, 128);
         mbar_init(&bars->mma_done, 1);
         bars->abort = 0;
         fence_mbar_init();
