@@ -183,8 +183,8 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
             mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(b0, kk * 16 * 128), idQ, kk > 0);
     };
 
-    bool ok = mbar_wait(&bars->kv_full, 0, abort_flag) && mbar_wait(&bars->qdo_full[0], 0, abort_flag) &&
-              mbar_wait(&bars->ka_ready, 0, abort_flag);
+    bool ok = mbar_wait_poll(&bars->kv_full, 0, abort_flag) && mbar_wait_poll(&bars->qdo_full[0], 0, abort_flag) &&
+              mbar_wait_poll(&bars->ka_ready, 0, abort_flag);
     if (ok) {
         tc_fence_after();
         s_mma(kQ, C::col_s(0));
@@ -197,17 +197,17 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         const int s1 = (i + 1) % kStages;
         const int buf = i & 1;
         if (i + 1 < Tq) {
-            if (!(ok = mbar_wait(&bars->qdo_full[s1], ((i + 1) / kStages) & 1, abort_flag))) break;
+            if (!(ok = mbar_wait_poll(&bars->qdo_full[s1], ((i + 1) / kStages) & 1, abort_flag))) break;
             // Buffer buf^1 last held dQ^T of step i-1: it must have been drained.
-            if (i > 0 && !(ok = mbar_wait(&bars->dq_empty, (i - 1) & 1, abort_flag))) break;
+            if (i > 0 && !(ok = mbar_wait_poll(&bars->dq_empty, (i - 1) & 1, abort_flag))) break;
             tc_fence_after();
             s_mma(sdesc_advance(kQ, s1 * C::kQBytes), C::col_s(buf ^ 1));
             mma_commit(&bars->s_full[buf ^ 1]);
         }
-        if (!(ok = mbar_wait(&bars->p_ready, i & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_poll(&bars->p_ready, i & 1, abort_flag))) break;
         tc_fence_after();
         grad(C::col_s(buf), sdesc_advance(mDO, s * C::kQBytes), C::kColDV, i > 0);
-        if (!(ok = mbar_wait(&bars->ds_ready, i & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_poll(&bars->ds_ready, i & 1, abort_flag))) break;
         tc_fence_after();
         grad(C::kColDP, sdesc_advance(mQ, s * C::kQBytes), C::kColDK, i > 0);
         mma_commit(&bars->qdo_empty[s]);

@@ -139,12 +139,12 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
             mma_ts(d, a + kk * 8, sdesc_advance(b0, kk * 16 * 128), idPV, (accumulate || kk > 0) ? 1u : 0u);
     };
 
-    bool ok = mbar_wait(&bars->q_full[0], 0, abort_flag) && mbar_wait(&bars->q_full[1], 0, abort_flag);
+    bool ok = mbar_wait_poll(&bars->q_full[0], 0, abort_flag) && mbar_wait_poll(&bars->q_full[1], 0, abort_flag);
     for (int j = 0; ok && j < T; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
         if (j == 0) {
-            if (!(ok = mbar_wait(&bars->k_full[s], ph, abort_flag))) break;
+            if (!(ok = mbar_wait_poll(&bars->k_full[s], ph, abort_flag))) break;
             tc_fence_after();
             issue_s(0, s);
             mma_commit(&bars->s_full[0]);
@@ -153,18 +153,18 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
         }
         const int s2 = (j + 1) % C::kStages;
         const uint32_t ph2 = ((j + 1) / C::kStages) & 1;
-        if (!(ok = mbar_wait(&bars->v_full[s], ph, abort_flag))) break;
-        if (!(ok = mbar_wait(&bars->p_full[0], j & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_poll(&bars->v_full[s], ph, abort_flag))) break;
+        if (!(ok = mbar_wait_poll(&bars->p_full[0], j & 1, abort_flag))) break;
         tc_fence_after();
         issue_pv(0, s, j > 0);
         if (j == T - 1) mma_commit(&bars->o_full[0]);
         if (j + 1 < T) {
-            if (!(ok = mbar_wait(&bars->k_full[s2], ph2, abort_flag))) break;
+            if (!(ok = mbar_wait_poll(&bars->k_full[s2], ph2, abort_flag))) break;
             tc_fence_after();
             issue_s(0, s2);
             mma_commit(&bars->s_full[0]);
         }
-        if (!(ok = mbar_wait(&bars->p_full[1], j & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_poll(&bars->p_full[1], j & 1, abort_flag))) break;
         tc_fence_after();
         issue_pv(1, s, j > 0);
         mma_commit(&bars->kv_empty[s]);
@@ -207,11 +207,17 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
                 for (int c = 0; c < 32; ++c)
                     if (q * 32 + c >= tail) r[q][c] = __float_as_uint(-INFINITY);
         }
-        float mx = -INFINITY;
+        // Row max as eight independent chains of 3-input maxima: with two warps per scheduler there is
+        // nothing else to hide a 128-long dependent chain behind.
+        float mc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mc[k] = -INFINITY;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
 #pragma unroll
-            for (int c = 0; c < 32; ++c) mx = fmaxf(mx, __uint_as_float(r[q][c]));
+            for (int c = 0; c < 32; c += 2)
+                mc[(c / 2) % 8] = max3(mc[(c / 2) % 8], __uint_as_float(r[q][c]), __uint_as_float(r[q][c + 1]));
+        const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
         const float m_new = fmaxf(m_run, mx * scale_log2);
         const bool rescale = m_new - m_run > kRescaleThreshold;  // always true for the first block
         float alpha = 1.f;
@@ -220,7 +226,9 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
             m_run = m_new;
         }
         const float neg_m = -m_run;
-        float sum = 0.f;
+        float sc[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) sc[k] = 0.f;
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t pk[32];
@@ -228,11 +236,12 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
             for (int c = 0; c < 32; ++c) {
                 const float p0 = ex2(fmaf(__uint_as_float(r[2 * h + c / 16][(2 * c) % 32]), scale_log2, neg_m));
                 const float p1 = ex2(fmaf(__uint_as_float(r[2 * h + c / 16][(2 * c + 1) % 32]), scale_log2, neg_m));
-                sum += p0 + p1;
+                sc[c % 8] += p0 + p1;
                 pk[c] = pack_bf16(p0, p1);
             }
             tmem_st32(tS + h * 32, pk);
         }
+        const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
         l_run = l_run * alpha + sum;
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
 #pragma unroll

@@ -39,6 +39,18 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Clock budget of one wait: about two seconds at the GB300's clocks.  A wait that runs out of it
 // reports a timeout instead of spinning forever.
 constexpr long long kWaitBudgetCycles = 4000000000LL;
@@ -50,6 +62,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     const long long t0 = clock64();
     while (true) {
         if (mbar_test(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitBudgetCycles) {
+            *abort_flag = 1;
+            return false;
+        }
+    }
+}
+
+// As mbar_wait, but polls without suspending.  For the single MMA-issuing thread: a suspended
+// try_wait was measured to notice a completed phase some 400 cycles late, and the tensor core idles
+// for that long; one polling thread costs the other warps little issue bandwidth.
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_poll(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (true) {
+        if (mbar_poll(bar, parity)) return true;
         if (*abort_flag) return false;
         if (clock64() - t0 > kWaitBudgetCycles) {
             *abort_flag = 1;
@@ -232,6 +260,12 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+// Three-input maximum (one instruction on sm_100-class GPUs).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
 }
 // Packs (lo, hi) into one 32-bit word of two bf16 (round to nearest even); lo in the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
