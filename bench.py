@@ -37,6 +37,16 @@ def _dist_env():
     return rank, world, local
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """Largest value of `x` over all ranks (timings are reported for the slowest rank)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -102,25 +112,22 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _oracle_sample(w, rows: int, inp):
-    """fp64 oracle forward + backward for one head with `rows` query rows against all N keys."""
+def _oracle_sample(w, heads: int, inp):
+    """fp64 oracle forward + backward of the first `heads` heads of batch 0, full N x N each."""
     import oracle
-    q = inp["q"][:1, :1, :rows].double().numpy()
-    k = inp["k"][:1, :1].double().numpy()
-    v = inp["v"][:1, :1].double().numpy()
-    do = inp["do"][:1, :1, :rows].double().numpy()
+    q, k, v, do = (inp[n][:1, :heads].double().numpy() for n in ("q", "k", "v", "do"))
     t0 = time.perf_counter()
     oracle.forward(q, k, v, w.scale)
     oracle.backward(q, k, v, do, w.scale)
     dt = time.perf_counter() - t0
-    flops = 14.0 * rows * w.N * w.d
+    flops = 14.0 * heads * w.N * w.N * w.d
     return flops, dt
 
 
-def _cpu_meta(rows, w):
+def _cpu_meta(heads, w):
     return {"kind": "oracle", "cores": _NCPU,
-            "sample": f"fp64 oracle forward+backward of head 0 with {rows} of {w.N} query rows against all "
-                      f"{w.N} keys (d={w.d}); flops counted as 14*rows*N*d"}
+            "sample": f"fp64 oracle (numpy, {_NCPU} BLAS threads) forward+backward of {heads} of the {w.B * w.H} "
+                      f"heads (N={w.N}, d={w.d}), all rows; flops counted as 14*heads*N^2*d"}
 
 
 def run_reference(args, w):
@@ -128,16 +135,16 @@ def run_reference(args, w):
     if rank != 0:
         return 0
     inp = fa_inputs.workload_inputs(w, with_grad=True)
-    rows = args.oracle_rows
+    heads = args.oracle_heads_per_step
     for _ in range(args.warmup):
-        _oracle_sample(w, rows, inp)
+        _oracle_sample(w, heads, inp)
     total_f, total_t = 0.0, 0.0
     for _ in range(args.steps):
-        f, t = _oracle_sample(w, rows, inp)
+        f, t = _oracle_sample(w, heads, inp)
         total_f += f
         total_t += t
     tflops = total_f / total_t / 1e12
-    meta = _cpu_meta(rows, w)
+    meta = _cpu_meta(heads, w)
     meta["value"] = tflops
     meta["unit"] = "TFLOP/s"
     line = {"impl": "reference", "metric": METRIC, "value": tflops, "unit": "TFLOP/s", "n_gpus": args.gpus,
@@ -213,10 +220,7 @@ def run_ours(args, w):
     fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     step_ms = sum(fwd_ms) / args.steps + sum(bwd_ms) / args.steps
-    if world > 1:
-        t = torch.tensor([step_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_ms = float(t.item())
+    step_ms = max_over_ranks(step_ms, dev)
     total_flops = (w.fwd_flops() + w.bwd_flops()) * world
     value = total_flops / (step_ms * 1e-3) / 1e12
     fwd_avg = sum(fwd_ms) / args.steps
@@ -226,36 +230,8 @@ def run_ours(args, w):
     peaks = _peaks()
     peak = peaks["bf16_tflops"]
 
-    # End to end through the public API: pinned host inputs in, gradients and O back to pinned host memory.
-    host_in = {n: inp_cpu[n].pin_memory() for n in ("q", "k", "v", "do")}
-    host_out = {n: torch.empty_like(inp_cpu["q"]).pin_memory() for n in ("o", "dq", "dk", "dv")}
-    host_lse = torch.empty(B, H, N, dtype=torch.float32).pin_memory()
-
-    def e2e_step():
-        for n, t in (("q", q), ("k", k), ("v", v), ("do", do)):
-            t.copy_(host_in[n], non_blocking=True)
-        step()
-        for n, t in (("o", o), ("dq", dq), ("dk", dk), ("dv", dv)):
-            host_out[n].copy_(t, non_blocking=True)
-        host_lse.copy_(lse, non_blocking=True)
-
-    e2e_steps = max(3, args.steps // 2)
-    e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    elt = q.element_size() * q.numel()
-    h2d = 4 * elt
-    d2h = 4 * elt + host_lse.numel() * 4
+    e2e_ms, h2d, d2h = _e2e(fa, w, inp_cpu, dev, args.steps)
+    e2e_ms = max_over_ranks(e2e_ms, dev)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -269,13 +245,15 @@ def run_ours(args, w):
         "clocks": clk,
         "gpu_launches": args.steps * LAUNCHES_PER_STEP,
         "e2e": {"value": (w.fwd_flops() + w.bwd_flops()) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
-                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "pinned host q,k,v,dO copied in and o,lse,dq,dk,dv copied out every step, through the "
+                       "public API; copies run on two copy streams, double-buffered so that step i's "
+                       "transfers overlap steps i-1 and i+1's compute"},
     }
     line["roofline"] = _roofline(w, fwd_avg, bwd_avg, peaks)
     if rank == 0 and not args.no_cpu_baseline:
-        rows = args.oracle_rows
-        f, t = _oracle_sample(w, rows, inp_cpu)
-        meta = _cpu_meta(rows, w)
+        f, t = _oracle_sample(w, args.oracle_heads, inp_cpu)
+        meta = _cpu_meta(args.oracle_heads, w)
         meta.update({"value": f / t / 1e12, "unit": "TFLOP/s", "seconds": t})
         line["cpu_baseline"] = meta
     if rank == 0:
@@ -285,8 +263,69 @@ def run_ours(args, w):
     return 0
 
 
+def _e2e(fa, w, inp_cpu, dev, steps):
+    """Per-step time of fa_fwd + fa_bwd fed from and drained to pinned host memory (double-buffered)."""
+    B, H, N, d = w.B, w.H, w.N, w.d
+    host_in = {n: inp_cpu[n].pin_memory() for n in ("q", "k", "v", "do")}
+    host_out = [{n: torch.empty(B, H, N, d, dtype=inp_cpu["q"].dtype).pin_memory() for n in ("o", "dq", "dk", "dv")}
+                for _ in range(2)]
+    for h in host_out:
+        h["lse"] = torch.empty(B, H, N, dtype=torch.float32).pin_memory()
+    bufs = []
+    for _ in range(2):
+        b = {n: torch.empty(B, H, N, d, dtype=inp_cpu["q"].dtype, device=dev) for n in ("q", "k", "v", "do", "o", "dq", "dk", "dv")}
+        b["lse"] = torch.empty(B, H, N, dtype=torch.float32, device=dev)
+        b["ws"] = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+        bufs.append(b)
+    comp = torch.cuda.current_stream(dev)
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    free = [torch.cuda.Event() for _ in range(2)]
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    computed = [torch.cuda.Event() for _ in range(2)]
+    for e in free:
+        e.record(comp)
+
+    def run(n):
+        for i in range(n):
+            j = i % 2
+            b, ho = bufs[j], host_out[j]
+            h2d_s.wait_event(free[j])
+            with torch.cuda.stream(h2d_s):
+                for name in ("q", "k", "v", "do"):
+                    b[name].copy_(host_in[name], non_blocking=True)
+                loaded[j].record(h2d_s)
+            comp.wait_event(loaded[j])
+            fa.fa_fwd(b["q"], b["k"], b["v"], w.scale, b["o"], b["lse"], stream=comp)
+            fa.fa_bwd(b["q"], b["k"], b["v"], b["o"], b["do"], b["lse"], w.scale, b["dq"], b["dk"], b["dv"], b["ws"],
+                      stream=comp)
+            computed[j].record(comp)
+            d2h_s.wait_event(computed[j])
+            with torch.cuda.stream(d2h_s):
+                for name in ("o", "lse", "dq", "dk", "dv"):
+                    ho[name].copy_(b[name], non_blocking=True)
+                free[j].record(d2h_s)
+
+    run(4)
+    torch.cuda.synchronize(dev)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(comp)
+    h2d_s.wait_stream(comp)
+    run(steps)
+    comp.wait_stream(d2h_s)
+    end.record(comp)
+    torch.cuda.synchronize(dev)
+    elt = inp_cpu["q"].element_size() * inp_cpu["q"].numel()
+    return start.elapsed_time(end) / steps, 4 * elt, 4 * elt + B * H * N * 4
+
+
 # Kernels launched per step: the forward kernel, and the backward's row-term, main and dQ kernels.
 LAUNCHES_PER_STEP = 4
+
+
+# DRAM bytes per launch of the dominant kernel at the bench workload, from one ncu capture of the
+# kernel as it is built now (profiles/dram_per_launch_bench_B1-H16-N8192-d128.md).  Set to None whenever
+# the kernel changes until it is measured again.
+TRAFFIC_BYTES = {("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): 202424832 + 83024896}
 
 
 def _roofline(w, fwd_ms, bwd_ms, peaks):
@@ -298,7 +337,8 @@ def _roofline(w, fwd_ms, bwd_ms, peaks):
     achieved = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
     return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "peak_source": f"{peaks['source']} burst bf16 (cuBLAS)", "traffic": None}
+            "frac": achieved / peak, "peak_source": f"{peaks['source']} burst bf16 (cuBLAS)",
+            "traffic": TRAFFIC_BYTES.get((name, w.name)), "traffic_unit": "bytes per launch (bwd_tc_kernel, ncu)"}
 
 
 def main():
@@ -308,7 +348,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=fa_inputs.HEADLINE, choices=sorted(fa_inputs.WORKLOADS))
-    ap.add_argument("--oracle-rows", type=int, default=512)
+    ap.add_argument("--oracle-heads", type=int, default=8,
+                    help="heads of the workload the CPU baseline runs through the oracle (about 1.5 s each)")
+    ap.add_argument("--oracle-heads-per-step", type=int, default=1,
+                    help="heads per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     w = fa_inputs.WORKLOADS[args.workload]
