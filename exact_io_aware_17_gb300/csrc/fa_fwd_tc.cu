@@ -226,21 +226,27 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
             m_run = m_new;
         }
         const float neg_m = -m_run;
-        float sc[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) sc[k] = 0.f;
+        // s * scale*log2e - m and the row sum run on packed pairs (f32x2): two results per instruction.
+        const uint64_t sl2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(neg_m, neg_m);
+        uint64_t s2[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; ++c) {
-                const float p0 = ex2(fmaf(__uint_as_float(r[2 * h + c / 16][(2 * c) % 32]), scale_log2, neg_m));
-                const float p1 = ex2(fmaf(__uint_as_float(r[2 * h + c / 16][(2 * c + 1) % 32]), scale_log2, neg_m));
-                sc[c % 8] += p0 + p1;
+                const int q = 2 * h + c / 16, e = (2 * c) % 32;
+                const uint64_t x2 = ffma2(f2_pack(__uint_as_float(r[q][e]), __uint_as_float(r[q][e + 1])), sl2, nm2);
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                const float p0 = ex2(x0), p1 = ex2(x1);
+                s2[c % 4] = fadd2(s2[c % 4], f2_pack(p0, p1));
                 pk[c] = pack_bf16(p0, p1);
             }
             tmem_st32(tS + h * 32, pk);
         }
+        float sc[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) f2_unpack(s2[k], sc[2 * k], sc[2 * k + 1]);
         const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
         l_run = l_run * alpha + sum;
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
