@@ -7,15 +7,16 @@
 //     dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three kernels per call:
-//   bwd_prep_kernel   D_i and LSE_i * log2(e) per query row (padded to a multiple of 64 rows per head,
-//                     pad rows get D = 0 and LSE = +inf so they contribute nothing), and zeroes the
-//                     fp32 dQ accumulator.
+//   bwd_prep_kernel   -D_i and -LSE_i * log2(e) per query row (padded to a multiple of 64 rows per head;
+//                     pad rows get 0 and -inf so they contribute nothing), and zeroes the fp32 dQ
+//                     accumulator.  Negated so that the main kernel applies them with packed-pair adds.
 //   bwd_tc_kernel     one CTA per (head, block of 128 keys).  K_j, V_j stay in shared memory; the CTA
 //                     walks every block of 64 queries i:
 //                         S^T  = K_j Q_i^T            K_j as bf16 from tensor memory; fp32 result,
 //                                                     double buffered
 //                         dP^T = V_j dO_i^T
-//                         P^T  = exp2(S^T scale log2e - LSE2_i)    thread = key row
+//                         P^T  = exp2(S^T scale log2e - LSE2_i)    thread = key row; packed fp32
+//                                                     pairs (f32x2) for the element-wise work
 //                         dS^T = P^T o (dP^T - D_i)
 //                         dV_j += P^T dO_i            P^T as bf16 from tensor memory
 //                         dK_j += dS^T Q_i            dS^T as bf16 from tensor memory
@@ -271,16 +272,21 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, __
         tmem_ld32(tmem + lane_off + C::col_s(buf), sr[0]);
         tmem_ld32(tmem + lane_off + C::col_s(buf) + 32, sr[1]);
         tmem_ld_wait();
-        float p[BQ];
-#pragma unroll
-        for (int c = 0; c < BQ; ++c) {
-            const float x = ex2(fmaf(__uint_as_float(sr[c / 32][c % 32]), scale_log2, -lse2[c]));
-            p[c] = valid_key ? x : 0.f;
-        }
+        uint64_t p2[BQ / 2];
         {
+            const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
             uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(p[2 * c], p[2 * c + 1]);
+            for (int c = 0; c < BQ / 2; ++c) {
+                const int q = (2 * c) / 32, e = (2 * c) % 32;
+                const uint64_t x2 = ffma2(f2_pack(__uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1])), sl2,
+                                          *reinterpret_cast<const uint64_t*>(lse2 + 2 * c));
+                float x0, x1;
+                f2_unpack(x2, x0, x1);
+                const float p0 = valid_key ? ex2(x0) : 0.f, p1 = valid_key ? ex2(x1) : 0.f;
+                p2[c] = f2_pack(p0, p1);
+                pk[c] = pack_bf16(p0, p1);
+            }
             tmem_st32(tmem + lane_off + C::col_s(buf), pk);
         }
         tmem_st_wait();
@@ -296,8 +302,11 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, __
         uint32_t pk[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
-            const float d0 = p[2 * c] * (__uint_as_float(dr[(2 * c) / 32][(2 * c) % 32]) - drow[2 * c]);
-            const float d1 = p[2 * c + 1] * (__uint_as_float(dr[(2 * c + 1) / 32][(2 * c + 1) % 32]) - drow[2 * c + 1]);
+            const int q = (2 * c) / 32, e = (2 * c) % 32;
+            const uint64_t g2 = fadd2(f2_pack(__uint_as_float(dr[q][e]), __uint_as_float(dr[q][e + 1])),
+                                      *reinterpret_cast<const uint64_t*>(drow + 2 * c));
+            float d0, d1;
+            f2_unpack(fmul2(p2[c], g2), d0, d1);
             pk[c] = pack_bf16(d0, d1);
         }
         tmem_st32(tmem + lane_off + C::kColDP, pk);
@@ -465,7 +474,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (threadIdx.x == 0 && bars->abort) atomicCAS(&g_bwd_status, 0, (int)FA_ERR_TIMEOUT);
 }
 
-// D_i = dO_i . O_i and LSE2_i = LSE_i log2(e) into [head][Npad] arrays (pad rows: D = 0, LSE2 = +inf);
+// -D_i = -(dO_i . O_i) and -LSE2_i = -LSE_i log2(e) into [head][Npad] arrays (pad rows: 0 and -inf);
 // zeroes the fp32 dQ accumulator.  One warp per (padded) row, grid-stride.
 __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                 const float* __restrict__ lse, float* __restrict__ row_d, float* __restrict__ lse2,
@@ -479,7 +488,7 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_
         if (r >= N) {
             if (lane == 0) {
                 row_d[w] = 0.f;
-                lse2[w] = INFINITY;
+                lse2[w] = -INFINITY;
             }
             continue;
         }
@@ -500,8 +509,8 @@ __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_
         }
         for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
         if (lane == 0) {
-            row_d[w] = acc;
-            lse2[w] = lse[(size_t)h * N + r] * 1.4426950408889634f;
+            row_d[w] = -acc;
+            lse2[w] = -lse[(size_t)h * N + r] * 1.4426950408889634f;
         }
     }
     const int64_t n4 = heads * (int64_t)N * d / 4;

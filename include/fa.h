@@ -69,9 +69,9 @@ fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, f
 
 /*
  * fa_bwd_workspace_size — bytes of device scratch fa_bwd needs for this shape: an fp32 dQ accumulator
- * [B,H,N,d] and two fp32 per-row arrays [B,H,Np] with Np = N rounded up to a multiple of 64 (the row
- * term D_i = dO_i . O_i and the log2-domain LSE), each section rounded up to 256 bytes.  Returns 0
- * for invalid shapes.
+ * [B,H,N,d] and two fp32 per-row arrays [B,H,Np] with Np = N rounded up to a multiple of 64 (the
+ * negated row term -D_i = -dO_i . O_i and the negated log2-domain LSE), each section rounded up to 256
+ * bytes.  Returns 0 for invalid shapes.
  */
 size_t fa_bwd_workspace_size(int B, int H, int N, int d);
 
