@@ -325,7 +325,7 @@ LAUNCHES_PER_STEP = 4
 # DRAM bytes per launch of the dominant kernel at the bench workload, from one ncu capture of the
 # kernel as it is built now (profiles/dram_per_launch_bench_B1-H16-N8192-d128.md).  Set to None whenever
 # the kernel changes until it is measured again.
-TRAFFIC_BYTES = {}
+TRAFFIC_BYTES = {("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): 202448640 + 82996480}
 
 
 def _roofline(w, fwd_ms, bwd_ms, peaks):
