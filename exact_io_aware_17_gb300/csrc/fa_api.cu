@@ -3,6 +3,7 @@
 
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdlib.h>
 #include <stdarg.h>
 #include <stdio.h>
 
@@ -51,6 +52,12 @@ cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, 
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+WaitPolicy wait_policy() {
+    const char* v = getenv("FA_TEST_STARVE_WAIT");
+    if (v && v[0] == '1') return WaitPolicy{20000000LL, 1};  // ~10 ms, and the forward's Q loads withheld
+    return WaitPolicy{4000000000LL, 0};                       // ~2 s: no legitimate wait comes near it
 }
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }

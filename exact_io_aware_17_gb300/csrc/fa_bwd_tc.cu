@@ -404,7 +404,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const float* __restrict__ lse2, const float* __restrict__ row_d, float* __restrict__ dq_acc,
               __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int N, int Npad, float scale,
-              float scale_log2) {
+              float scale_log2, long long wait_budget) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -415,6 +415,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int Tq = Npad / BQ;
 
     if (threadIdx.x == 0) {
+        s_wait_budget = wait_budget;
         mbar_init(&bars->kv_full, 1);
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->qdo_full[s], 1);
@@ -569,7 +570,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     dim3 grid((s.N + BK - 1) / BK, (unsigned)s.heads());
     bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, lse2, row_d, dq_acc,
                                                             (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, s.N, Npad, scale,
-                                                            scale * 1.4426950408889634f);
+                                                            scale * 1.4426950408889634f, wait_policy().budget_cycles);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_dq_convert_kernel<<<blocks, 256, 0, st>>>(dq_acc, (__nv_bfloat16*)dq, scale, s.heads() * (int64_t)s.N * D / 4);
     return cudaGetLastError();

@@ -75,12 +75,14 @@ struct FwdCfg {
 
 template <int D>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint8_t* smem,
-                         FwdBarriers* bars, int head, int q0, int T) {
+                         FwdBarriers* bars, int head, int q0, int T, int starve) {
     using C = FwdCfg<D>;
     volatile int* abort_flag = &bars->abort;
     const uint64_t pol_kv = policy_evict_last();
     const uint64_t pol_q = policy_evict_first();
-    for (int t = 0; t < 2; ++t) {
+    // starve != 0 withholds the Q loads so that the MMA warp's first wait runs out: the failure path
+    // of the bounded waits, exercised by the tests with a short budget.
+    for (int t = 0; t < 2 && !starve; ++t) {
         mbar_expect_tx(&bars->q_full[t], C::kQBytes);
         for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffQ + t * C::kQBytes + c * C::kChunkQ, tm_q, &bars->q_full[t], c * 64,
@@ -293,7 +295,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-              int N, float scale_log2) {
+              int N, float scale_log2, long long wait_budget, int starve) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -304,6 +306,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int T = (N + BN - 1) / BN;
 
     if (threadIdx.x == 0) {
+        s_wait_budget = wait_budget;
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->q_full[t], 1);
             mbar_init(&bars->s_full[t], 1);
@@ -334,7 +337,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == kTmaWarp) {
-        if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, smem, bars, head, q0, T);
+        if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, smem, bars, head, q0, T, starve);
     } else if (warp == kMmaWarp) {
         if (lane == 0) mma_issuer<D>(smem, bars, tmem, T);
     } else {
@@ -363,7 +366,9 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
     if (e != cudaSuccess) return e;
     dim3 grid((s.N + 2 * BM - 1) / (2 * BM), (unsigned)s.heads());
     const float scale_log2 = scale * 1.4426950408889634f;
-    fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, s.N, scale_log2);
+    const WaitPolicy wp = wait_policy();
+    fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, s.N, scale_log2,
+                                                            wp.budget_cycles, wp.starve);
     return cudaGetLastError();
 }
 

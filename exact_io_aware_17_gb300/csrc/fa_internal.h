@@ -33,6 +33,14 @@ BwdWorkspace bwd_workspace_layout(const Shape& s);
 // Rows per head of the backward's per-row arrays: N rounded up to the 64-query block of the kernel.
 inline int bwd_padded_rows(int N) { return (N + 63) / 64 * 64; }
 
+// Budget of the kernels' bounded waits, and the test switch that makes the forward's first wait run
+// out (FA_TEST_STARVE_WAIT=1 in the environment: the Q loads are withheld and the budget is ~10 ms).
+struct WaitPolicy {
+    long long budget_cycles;
+    int starve;
+};
+WaitPolicy wait_policy();
+
 // Encodes a TMA descriptor for a bf16 [heads, N, d] array (d innermost) with boxes of 64 columns x
 // `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows);

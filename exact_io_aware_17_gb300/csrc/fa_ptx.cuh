@@ -52,8 +52,10 @@ __device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
 }
 
 // Clock budget of one wait: about two seconds at the GB300's clocks.  A wait that runs out of it
-// reports a timeout instead of spinning forever.
+// reports a timeout instead of spinning forever.  Each kernel copies its budget (normally this value;
+// shorter in the tests that make a wait run out on purpose) into s_wait_budget before any wait.
 constexpr long long kWaitBudgetCycles = 4000000000LL;
+static __shared__ long long s_wait_budget;
 
 // Waits for the phase with the given parity to complete.  Returns false if the budget ran out or
 // `abort_flag` (shared) became nonzero; the caller then winds down.
@@ -63,7 +65,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     while (true) {
         if (mbar_test(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitBudgetCycles) {
+        if (clock64() - t0 > s_wait_budget) {
             *abort_flag = 1;
             return false;
         }
@@ -79,7 +81,7 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, v
     while (true) {
         if (mbar_poll(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitBudgetCycles) {
+        if (clock64() - t0 > s_wait_budget) {
             *abort_flag = 1;
             return false;
         }
@@ -95,7 +97,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // Waits with a fixed budget and no abort check: used to drain copies in flight before exit.
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
     const long long t0 = clock64();
-    while (!mbar_test(bar, parity) && clock64() - t0 < kWaitBudgetCycles) {
+    while (!mbar_test(bar, parity) && clock64() - t0 < s_wait_budget) {
     }
 }
 

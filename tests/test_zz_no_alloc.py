@@ -40,11 +40,14 @@ def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row(shape):
     ref = fa.fa_bwd(q, k, v, o, do, lse, scale)
     outs = [tuple(torch.empty_like(q) for _ in range(3)) for _ in range(2)]
     torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
     before = torch.cuda.memory_allocated()
     for dq, dk, dv in outs:                         # two calls in a row on the shared static scratch
         fa.fa_bwd_noalloc(q, k, v, o, do, lse, scale, dq, dk, dv)
     torch.cuda.synchronize()
-    assert torch.cuda.memory_allocated() == before   # no torch allocation during the calls
+    # No torch allocation during the calls: the peak never rose above what was allocated before them
+    # (the current figure may drop if the collector frees an unrelated tensor meanwhile).
+    assert torch.cuda.max_memory_allocated() <= before
     fa.fa_check_status()
     for got in outs:
         for g, r in zip(got, ref):
