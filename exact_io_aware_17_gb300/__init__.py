@@ -19,7 +19,7 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = ran
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA", 4: "FA_ERR_TIMEOUT"}
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc", "fa_last_error_string",
+EXPORTS = ("fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc", "fa_last_error_string",
            "fa_check_status")
 
 # Bytes of the static scratch that fa_bwd_noalloc uses (FA_BWD_NOALLOC_MAX_SCRATCH_BYTES).
@@ -45,6 +45,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
     lib.fa_fwd.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
     lib.fa_fwd.restype = I
+    lib.fa_fwd_stepnorm.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
+    lib.fa_fwd_stepnorm.restype = I
     lib.fa_fwd_f32.argtypes = [P, P, P, P, P, I, I, I, I, F, P]
     lib.fa_fwd_f32.restype = I
     lib.fa_bwd_workspace_size.argtypes = [I, I, I, I]
@@ -92,7 +94,7 @@ def _check_tensor(name, t, shape, dtype):
         raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor of shape {tuple(shape)}")
 
 
-def fa_fwd(q, k, v, scale=None, o=None, lse=None, stream=None):
+def fa_fwd(q, k, v, scale=None, o=None, lse=None, stream=None, _entry="fa_fwd"):
     """bf16 forward: returns (o bf16 [B,H,N,d], lse fp32 [B,H,N])."""
     B, H, N, d = _shape(q)
     for name, t in (("q", q), ("k", k), ("v", v)):
@@ -101,9 +103,14 @@ def fa_fwd(q, k, v, scale=None, o=None, lse=None, stream=None):
     lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
     _check_tensor("o", o, (B, H, N, d), torch.bfloat16)
     _check_tensor("lse", lse, (B, H, N), torch.float32)
-    _check(load_library().fa_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                 _default_scale(d, scale), _stream(stream)))
+    _check(getattr(load_library(), _entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                           _default_scale(d, scale), _stream(stream)))
     return o, lse
+
+
+def fa_fwd_stepnorm(q, k, v, scale=None, o=None, lse=None, stream=None):
+    """bf16 forward with the per-step normalised accumulator (ablation of fa_fwd's update rule)."""
+    return fa_fwd(q, k, v, scale, o, lse, stream, _entry="fa_fwd_stepnorm")
 
 
 def fa_fwd_f32(q, k, v, scale=None, o=None, lse=None, stream=None):
@@ -167,6 +174,6 @@ def fa_last_error_string() -> str:
     return load_library().fa_last_error_string().decode(errors="replace")
 
 
-__all__ = ["fa_fwd", "fa_fwd_f32", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc", "fa_check_status",
+__all__ = ["fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc", "fa_check_status",
            "fa_last_error_string",
            "load_library", "FAError", "EXPORTS", "LIB_PATH"]

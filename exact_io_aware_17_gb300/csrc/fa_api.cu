@@ -94,17 +94,27 @@ extern "C" {
 
 const char* fa_last_error_string(void) { return g_last_error; }
 
-fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
-                 int B, int H, int N, int d, float scale, void* stream) {
+static fa_status fwd_common(const char* fn, const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                            int H, int N, int d, float scale, void* stream, bool stepnorm) {
     g_last_error[0] = 0;
-    fa_status st = check_shape("fa_fwd", B, H, N, d, scale);
+    fa_status st = check_shape(fn, B, H, N, d, scale);
     if (st) return st;
     const void* ptrs[] = {q, k, v, o, lse};
     const char* names[] = {"q", "k", "v", "o", "lse"};
-    if ((st = check_ptrs("fa_fwd", ptrs, names, 5))) return st;
-    if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "fa_fwd: d must be 64 or 128 (got %d)", d);
+    if ((st = check_ptrs(fn, ptrs, names, 5))) return st;
+    if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "%s: d must be 64 or 128 (got %d)", fn, d);
     Shape s{B, H, N, d};
-    return launch_result("fa_fwd", launch_fwd_tc(q, k, v, o, lse, s, scale, (cudaStream_t)stream));
+    return launch_result(fn, launch_fwd_tc(q, k, v, o, lse, s, scale, (cudaStream_t)stream, stepnorm));
+}
+
+fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+                 int B, int H, int N, int d, float scale, void* stream) {
+    return fwd_common("fa_fwd", q, k, v, o, lse, B, H, N, d, scale, stream, false);
+}
+
+fa_status fa_fwd_stepnorm(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int N, int d, float scale, void* stream) {
+    return fwd_common("fa_fwd_stepnorm", q, k, v, o, lse, B, H, N, d, scale, stream, true);
 }
 
 fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, float* lse,

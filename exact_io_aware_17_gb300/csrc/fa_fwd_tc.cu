@@ -15,6 +15,12 @@
 // more than 2^8 (in the log2 domain).  O and l always share that reference, so O / l and
 // m + ln l are unchanged; the skipped rescales only bound P by 256 instead of 1.
 //
+// kStepNorm (fa_fwd_stepnorm) instead keeps O normalised after every block, the per-step update rule
+// that "账房先生的奔命" §六 prints:  O_new = exp(m_old - m_new) (l_old / l_new) O_old + exp(S - m_new) V / l_new.
+// P is divided by l_new before the MMA, O is rescaled in tensor memory on every block, and nothing is
+// divided at the end.  It gives the same results up to rounding and exists to measure what the
+// unnormalised accumulator saves.
+//
 // Warp roles (320 threads): warps 0-3 own Q0's rows, warps 4-7 own Q1's rows (thread = row = TMEM
 // lane), warp 8 issues TMA loads, warp 9 allocates TMEM and issues the MMAs.  While one warpgroup
 // exponentiates its S tile the tensor cores run the other tile's MMAs.
@@ -181,7 +187,7 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
     drain_wait(&bars->mma_done, 0);
 }
 
-template <int D>
+template <int D, bool kStepNorm>
 __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat16* __restrict__ o,
                            float* __restrict__ lse, int head, int q0, int N, int T, float scale_log2) {
     using C = FwdCfg<D>;
@@ -220,6 +226,56 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
             for (int c = 0; c < 32; c += 2)
                 mc[(c / 2) % 8] = max3(mc[(c / 2) % 8], __uint_as_float(r[q][c]), __uint_as_float(r[q][c + 1]));
         const float mx = max3(max3(mc[0], mc[1], mc[2]), max3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+        if constexpr (kStepNorm) {
+            const float m_new = fmaxf(m_run, mx * scale_log2);
+            const float alpha = ex2(m_run - m_new);  // 0 on the first block (m_run = -inf)
+            m_run = m_new;
+            const uint64_t sl2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(-m_run, -m_run);
+            uint64_t s2[4] = {0, 0, 0, 0};
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int e = 0; e < 32; e += 2) {
+                    float x0, x1;
+                    f2_unpack(ffma2(f2_pack(__uint_as_float(r[q][e]), __uint_as_float(r[q][e + 1])), sl2, nm2), x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    s2[(e / 2) % 4] = fadd2(s2[(e / 2) % 4], f2_pack(p0, p1));
+                    r[q][e] = __float_as_uint(p0);
+                    r[q][e + 1] = __float_as_uint(p1);
+                }
+            float sc[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) f2_unpack(s2[k], sc[2 * k], sc[2 * k + 1]);
+            const float l_new = alpha * l_run + (((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7])));
+            const float inv = 1.f / l_new;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t pk[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    const int q = 2 * h + c / 16, e = (2 * c) % 32;
+                    pk[c] = pack_bf16(__uint_as_float(r[q][e]) * inv, __uint_as_float(r[q][e + 1]) * inv);
+                }
+                tmem_st32(tS + h * 32, pk);
+            }
+            if (j > 0) {
+                const float c_old = alpha * l_run * inv;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t x[32];
+                    tmem_ld32(tO + q * 32, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * c_old);
+                    tmem_st32(tO + q * 32, x);
+                }
+            }
+            l_run = l_new;
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[t]);
+            continue;
+        }
         const float m_new = fmaxf(m_run, mx * scale_log2);
         const bool rescale = m_new - m_run > kRescaleThreshold;  // always true for the first block
         float alpha = 1.f;
@@ -271,7 +327,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
     tc_fence_after();
 
     const int row = q0 + t * BM + quarter * 32 + lane;
-    const float inv_l = 1.f / l_run;
+    const float inv_l = kStepNorm ? 1.f : 1.f / l_run;
     const size_t base = ((size_t)head * N + row) * D;
 #pragma unroll
     for (int q = 0; q < D / 32; ++q) {
@@ -291,7 +347,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
     if (row < N) lse[(size_t)head * N + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
 }
 
-template <int D>
+template <int D, bool kStepNorm>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
@@ -341,7 +397,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     } else if (warp == kMmaWarp) {
         if (lane == 0) mma_issuer<D>(smem, bars, tmem, T);
     } else {
-        softmax_wg<D>(bars, tmem, warp / 4, o, lse, head, q0, N, T, scale_log2);
+        softmax_wg<D, kStepNorm>(bars, tmem, warp / 4, o, lse, head, q0, N, T, scale_log2);
     }
 
     tc_fence_before();
@@ -353,7 +409,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (threadIdx.x == 0 && bars->abort) atomicCAS(&g_fwd_status, 0, (int)FA_ERR_TIMEOUT);
 }
 
-template <int D>
+template <int D, bool kStepNorm>
 cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& s, float scale,
                    cudaStream_t st) {
     using C = FwdCfg<D>;
@@ -362,12 +418,12 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
     if ((e = make_tmap_bf16_3d(&tq, q, s.d, s.N, s.heads(), BM)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tk, k, s.d, s.N, s.heads(), BN)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BN)) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    e = cudaFuncSetAttribute(fwd_tc_kernel<D, kStepNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     dim3 grid((s.N + 2 * BM - 1) / (2 * BM), (unsigned)s.heads());
     const float scale_log2 = scale * 1.4426950408889634f;
     const WaitPolicy wp = wait_policy();
-    fwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, s.N, scale_log2,
+    fwd_tc_kernel<D, kStepNorm><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, s.N, scale_log2,
                                                             wp.budget_cycles, wp.starve);
     return cudaGetLastError();
 }
@@ -375,8 +431,12 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
 }  // namespace
 
 cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& s,
-                          float scale, cudaStream_t st) {
-    return s.d == 128 ? launch<128>(q, k, v, o, lse, s, scale, st) : launch<64>(q, k, v, o, lse, s, scale, st);
+                          float scale, cudaStream_t st, bool stepnorm) {
+    if (stepnorm)
+        return s.d == 128 ? launch<128, true>(q, k, v, o, lse, s, scale, st)
+                          : launch<64, true>(q, k, v, o, lse, s, scale, st);
+    return s.d == 128 ? launch<128, false>(q, k, v, o, lse, s, scale, st)
+                      : launch<64, false>(q, k, v, o, lse, s, scale, st);
 }
 
 int fwd_tc_read_and_clear_status(cudaStream_t st) {

@@ -47,7 +47,7 @@ cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, 
 
 // Launchers (return cudaGetLastError() of their launches).
 cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& s,
-                          float scale, cudaStream_t st);
+                          float scale, cudaStream_t st, bool stepnorm);
 cudaError_t launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                                 const Shape& s, float scale, cudaStream_t st);
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout,

@@ -50,6 +50,8 @@ def main():
     ap.add_argument("--d", type=int, nargs="+", default=[64, 128])
     ap.add_argument("--rows", type=int, default=131072, help="B*H*N of every shape")
     ap.add_argument("--iters", type=int, default=10)
+    ap.add_argument("--stepnorm", action="store_true",
+                    help="also time fa_fwd_stepnorm (the per-step normalised update rule)")
     a = ap.parse_args()
     peak, src = _peak()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
@@ -64,12 +66,15 @@ def main():
             ws = torch.empty(fa.fa_bwd_workspace_size(1, H, N, d), dtype=torch.uint8, device="cuda")
             tf = _time(lambda: fa.fa_fwd(q, k, v, scale, o, lse), flush, a.iters)
             tb = _time(lambda: fa.fa_bwd(q, k, v, o, do, lse, scale, dq, dk, dv, ws), flush, a.iters)
+            tsn = _time(lambda: fa.fa_fwd_stepnorm(q, k, v, scale, o, lse), flush, a.iters) if a.stepnorm else None
             fa.fa_check_status()
             ff = 4.0 * H * N * N * d
             line = {"B": 1, "H": H, "N": N, "d": d, "fwd_ms": tf, "fwd_tflops": ff / tf / 1e9,
                     "fwd_frac": ff / tf / 1e9 / peak, "bwd_ms": tb, "bwd_tflops": 2.5 * ff / tb / 1e9,
                     "bwd_frac": 2.5 * ff / tb / 1e9 / peak, "fwdbwd_tflops": 3.5 * ff / (tf + tb) / 1e9,
                     "fwdbwd_frac": 3.5 * ff / (tf + tb) / 1e9 / peak, "peak_tflops": peak, "peak_source": src}
+            if tsn is not None:
+                line.update(stepnorm_fwd_ms=tsn, stepnorm_fwd_tflops=ff / tsn / 1e9, stepnorm_slowdown=tsn / tf)
             print(json.dumps(line), flush=True)
             del q, k, v, do, o, lse, dq, dk, dv, ws
             torch.cuda.empty_cache()

@@ -59,6 +59,18 @@ fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* ls
                  int B, int H, int N, int d, float scale, void* stream);
 
 /*
+ * fa_fwd_stepnorm — fa_fwd with the per-step normalised accumulator, an ablation of the update rule.
+ *   Same arguments, layouts, results (up to rounding) and errors as fa_fwd.  After every K/V block the
+ *   output is kept normalised, O_new = exp(m_old - m_new) (l_old / l_new) O_old + exp(S - m_new) V / l_new,
+ *   the update rule printed in "账房先生的奔命：Flash Attention 与内存 I/O 革命" §六 (which that page calls a
+ *   simplified form); fa_fwd instead keeps the output unnormalised and divides once at the end (the
+ *   rescale of the FlashAttention fable on ckw19810413.github.io, 兩大核心魔法).  This entry point exists to
+ *   measure that difference: it rescales O in tensor memory on every block.
+ */
+fa_status fa_fwd_stepnorm(const void* q, const void* k, const void* v, void* o, float* lse,
+                          int B, int H, int N, int d, float scale, void* stream);
+
+/*
  * fa_fwd_f32 — fp32 forward on the CUDA cores (no tensor-core rounding of any operand).
  *   q, k, v, o : float [B,H,N,d];  lse : float [B,H,N].
  *   d          : 1 .. 128 and a multiple of 4 (FA_ERR_UNSUPPORTED otherwise).

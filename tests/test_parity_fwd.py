@@ -12,18 +12,18 @@ from parity_util import (TOL_F32, TOL_LSE_BF16, TOL_O_BF16, max_abs, need_gpu, n
 pytestmark = pytest.mark.gpu
 
 
-def _run_bf16(fa, inp, scale):
+def _run_bf16(fa, inp, scale, entry="fa_fwd"):
     q, k, v = (inp[n].cuda() for n in ("q", "k", "v"))
-    o, lse = fa.fa_fwd(q, k, v, scale)
+    o, lse = getattr(fa, entry)(q, k, v, scale)
     torch.cuda.synchronize()
     fa.fa_check_status()
     return o, lse
 
 
-def _check_full_bf16(fa, B, H, N, d, seed, q_gain=1.0):
+def _check_full_bf16(fa, B, H, N, d, seed, q_gain=1.0, entry="fa_fwd"):
     inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed, q_gain)
     scale = 1 / math.sqrt(d)
-    o, lse = _run_bf16(fa, inp, scale)
+    o, lse = _run_bf16(fa, inp, scale, entry)
     ro, rl = oracle.forward(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), scale)
     eo, el = max_abs(np64(o), ro), max_abs(np64(lse), rl)
     assert eo <= TOL_O_BF16, (B, H, N, d, eo)
@@ -161,3 +161,36 @@ def test_workload_b4_h16_n2048_d64_full():
 def test_workload_sampled_rows(name):
     fa = need_gpu()
     _sampled(fa, fa_inputs.WORKLOADS[name], 256)
+
+
+# --- the per-step normalised accumulator (fa_fwd_stepnorm): same results, different update rule --------
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("N", [1, 7, 129, 300, 1000])
+def test_stepnorm_ragged(N, d):
+    fa = need_gpu()
+    _check_full_bf16(fa, 1, 3, N, d, seed=1200 + N + d, entry="fa_fwd_stepnorm")
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_stepnorm_peaky_rows(d):
+    fa = need_gpu()
+    _check_full_bf16(fa, 1, 2, 1500, d, seed=1400 + d, q_gain=4.0, entry="fa_fwd_stepnorm")
+
+
+def test_stepnorm_agrees_with_fa_fwd_at_the_headline_shape():
+    """Both update rules on the B=1 H=16 N=8192 d=128 workload: sampled rows against the oracle, and the
+    two GPU results within the bf16 output tolerance of each other everywhere."""
+    fa = need_gpu()
+    w = fa_inputs.WORKLOADS["bf16-fwdbwd-B1-H16-N8192-d128"]
+    inp = fa_inputs.workload_inputs(w, with_grad=False)
+    o1, l1 = _run_bf16(fa, inp, w.scale, "fa_fwd")
+    o2, l2 = _run_bf16(fa, inp, w.scale, "fa_fwd_stepnorm")
+    assert (o1.float() - o2.float()).abs().max().item() <= TOL_O_BF16
+    assert (l1 - l2).abs().max().item() <= TOL_LSE_BF16
+    rows = fa_inputs.sample_rows(w.N, w.H, 64)
+    ro, rl = oracle.forward_rows(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), w.scale, [r.numpy() for r in rows])
+    go = np.stack([np64(o2[:, h, rows[h]]) for h in range(w.H)], axis=1)
+    gl = np.stack([np64(l2[:, h, rows[h]]) for h in range(w.H)], axis=1)
+    assert max_abs(go, ro) <= TOL_O_BF16
+    assert max_abs(gl, rl) <= TOL_LSE_BF16
