@@ -403,15 +403,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const float* __restrict__ lse2, const float* __restrict__ row_d, float* __restrict__ dq_acc,
-              __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int N, int Npad, float scale,
-              float scale_log2, long long wait_budget) {
+              __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int N, int Npad,
+              int blocks_per_head, float scale, float scale_log2, long long wait_budget) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(smem + C::kOffBar);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int head = blockIdx.y;
-    const int k0 = blockIdx.x * BK;
+    // 1-D grid, head-major: the CTAs of one head walk the same Q/dO blocks, which stay in L2.
+    const int head = blockIdx.x / blocks_per_head;
+    const int k0 = (blockIdx.x % blocks_per_head) * BK;
     const int Tq = Npad / BQ;
 
     if (threadIdx.x == 0) {
@@ -567,9 +568,11 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((s.N + BK - 1) / BK, (unsigned)s.heads());
+    const int bph = (s.N + BK - 1) / BK;
+    if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const unsigned grid = (unsigned)(bph * s.heads());
     bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, lse2, row_d, dq_acc,
-                                                            (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, s.N, Npad, scale,
+                                                            (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, s.N, Npad, bph, scale,
                                                             scale * 1.4426950408889634f, wait_policy().budget_cycles);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     bwd_dq_convert_kernel<<<blocks, 256, 0, st>>>(dq_acc, (__nv_bfloat16*)dq, scale, s.heads() * (int64_t)s.N * D / 4);

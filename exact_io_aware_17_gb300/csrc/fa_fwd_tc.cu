@@ -351,14 +351,15 @@ template <int D, bool kStepNorm>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-              int N, float scale_log2, long long wait_budget, int starve) {
+              int N, int blocks_per_head, float scale_log2, long long wait_budget, int starve) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     FwdBarriers* bars = reinterpret_cast<FwdBarriers*>(smem + C::kOffBar);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int head = blockIdx.y;
-    const int q0 = blockIdx.x * 2 * BM;
+    // 1-D grid, head-major: the CTAs of one head run together and share its K/V through L2.
+    const int head = blockIdx.x / blocks_per_head;
+    const int q0 = (blockIdx.x % blocks_per_head) * 2 * BM;
     const int T = (N + BN - 1) / BN;
 
     if (threadIdx.x == 0) {
@@ -420,10 +421,12 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BN)) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(fwd_tc_kernel<D, kStepNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
-    dim3 grid((s.N + 2 * BM - 1) / (2 * BM), (unsigned)s.heads());
+    const int bph = (s.N + 2 * BM - 1) / (2 * BM);
+    if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const unsigned grid = (unsigned)(bph * s.heads());
     const float scale_log2 = scale * 1.4426950408889634f;
     const WaitPolicy wp = wait_policy();
-    fwd_tc_kernel<D, kStepNorm><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, s.N, scale_log2,
+    fwd_tc_kernel<D, kStepNorm><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, s.N, bph, scale_log2,
                                                             wp.budget_cycles, wp.starve);
     return cudaGetLastError();
 }

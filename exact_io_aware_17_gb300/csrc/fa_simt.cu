@@ -50,11 +50,11 @@ __device__ __forceinline__ void stage_rows(float* dst, const T* src, int r0, int
 }
 
 // ---------------------------------------------------------------------------------------------
-// Forward.  grid = (ceil(N / (kWarps*kRows)), B*H), block = kWarps*32.
+// Forward.  grid = B*H*ceil(N / (kWarps*kRows)) (head-major), block = kWarps*32.
 template <typename T>
 __global__ void __launch_bounds__(kWarps * 32)
 fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                T* __restrict__ o, float* __restrict__ lse, int N, int d, float scale) {
+                T* __restrict__ o, float* __restrict__ lse, int N, int d, int blocks_per_head, float scale) {
     extern __shared__ float smem[];
     const int pitch = d + 1;
     float* ks = smem;                       // [kBlk][pitch]
@@ -62,15 +62,16 @@ fwd_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __res
     float* qs = vs + kBlk * pitch;          // [kWarps*kRows][d]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const size_t head = blockIdx.y;
+    const size_t head = blockIdx.x / blocks_per_head;
+    const int blk = blockIdx.x % blocks_per_head;
     const T* qh = q + head * N * d;
     const T* kh = k + head * N * d;
     const T* vh = v + head * N * d;
-    const int row0 = blockIdx.x * (kWarps * kRows) + warp * kRows;
+    const int row0 = blk * (kWarps * kRows) + warp * kRows;
 
     for (int idx = threadIdx.x; idx < kWarps * kRows * d; idx += blockDim.x) {
         int r = idx / d, c = idx - r * d;
-        int gr = blockIdx.x * (kWarps * kRows) + r;
+        int gr = blk * (kWarps * kRows) + r;
         qs[idx] = gr < N ? to_f(qh[(size_t)gr * d + c]) : 0.f;
     }
     const float* qw = qs + warp * kRows * d;
@@ -143,10 +144,12 @@ template <typename T>
 cudaError_t launch_fwd(const T* q, const T* k, const T* v, T* o, float* lse, const Shape& s,
                        float scale, cudaStream_t st) {
     const int rows_per_block = kWarps * kRows;
-    dim3 grid((s.N + rows_per_block - 1) / rows_per_block, (unsigned)s.heads());
+    const int bph = (s.N + rows_per_block - 1) / rows_per_block;
+    if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
+    const unsigned grid = (unsigned)(bph * s.heads());
     size_t smem = sizeof(float) * (2 * kBlk * (s.d + 1) + kWarps * kRows * s.d);
     cudaFuncSetAttribute(fwd_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    fwd_simt_kernel<T><<<grid, kWarps * 32, smem, st>>>(q, k, v, o, lse, s.N, s.d, scale);
+    fwd_simt_kernel<T><<<grid, kWarps * 32, smem, st>>>(q, k, v, o, lse, s.N, s.d, bph, scale);
     return cudaGetLastError();
 }
 

@@ -138,3 +138,15 @@ def test_bwd_long_sequences_sampled(N, d, q_gain):
     assert (dk_sum.abs() <= 2e-2 * dk.double().abs().sum(dim=2) + 1e-3).all()
     dv_err = dv.double().sum(dim=2) - inp["do"].double().sum(dim=2).cuda()
     assert (dv_err.abs() <= 2e-2 * dv.double().abs().sum(dim=2) + 1e-3).all()
+
+
+def test_bwd_more_heads_than_a_grid_dimension_holds():
+    fa = need_gpu()
+    B, H, N, d = 7, 10000, 5, 64
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed=4322, with_grad=True)
+    _, _, dq, dk, dv = _gpu_fwd_bwd(fa, inp, 0.125)
+    sel = [0, 4321, 69999]
+    sub = [inp[n].reshape(B * H, 1, N, d)[sel].transpose(0, 1) for n in ("q", "k", "v", "do")]
+    rq, rk, rv = oracle.backward(*(np64(t) for t in sub), 0.125)
+    for g, r in ((dq, rq), (dk, rk), (dv, rv)):
+        assert rel_fro(np64(g.reshape(B * H, N, d)[sel]), r[0]) <= TOL_GRAD_BF16

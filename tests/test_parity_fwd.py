@@ -194,3 +194,21 @@ def test_stepnorm_agrees_with_fa_fwd_at_the_headline_shape():
     gl = np.stack([np64(l2[:, h, rows[h]]) for h in range(w.H)], axis=1)
     assert max_abs(go, ro) <= TOL_O_BF16
     assert max_abs(gl, rl) <= TOL_LSE_BF16
+
+
+@pytest.mark.parametrize("entry", ["fa_fwd", "fa_fwd_f32"])
+def test_more_heads_than_a_grid_dimension_holds(entry):
+    """B*H = 70,000 short heads: more than the 65,535 CUDA allows in a grid's y dimension."""
+    fa = need_gpu()
+    B, H, N, d = 7, 10000, 3, 64
+    dtype = "bf16" if entry == "fa_fwd" else "f32"
+    inp = fa_inputs.make_inputs(B, H, N, d, dtype, seed=4321)
+    o, lse = getattr(fa, entry)(*(inp[n].cuda() for n in ("q", "k", "v")), 0.125)
+    torch.cuda.synchronize()
+    fa.fa_check_status()
+    sel = [0, 1234, 69999]
+    qf, kf, vf = (inp[n].reshape(B * H, 1, N, d)[sel].transpose(0, 1) for n in ("q", "k", "v"))
+    ro, rl = oracle.forward(np64(qf), np64(kf), np64(vf), 0.125)
+    tol_o, tol_l = (TOL_O_BF16, TOL_LSE_BF16) if entry == "fa_fwd" else (TOL_F32, TOL_F32)
+    assert max_abs(np64(o.reshape(B * H, N, d)[sel]), ro[0]) <= tol_o
+    assert max_abs(np64(lse.reshape(B * H, N)[sel]), rl[0]) <= tol_l
