@@ -51,10 +51,9 @@ __device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Clock budget of one wait: about two seconds at the GB300's clocks.  A wait that runs out of it
-// reports a timeout instead of spinning forever.  Each kernel copies its budget (normally this value;
-// shorter in the tests that make a wait run out on purpose) into s_wait_budget before any wait.
-constexpr long long kWaitBudgetCycles = 4000000000LL;
+// Clock budget of one wait, in cycles.  A wait that runs out of it reports a timeout instead of spinning
+// forever.  Each kernel copies the budget its launcher passes (about two seconds of clock normally;
+// ~10 ms in the tests that make a wait run out on purpose) into s_wait_budget before any wait.
 static __shared__ long long s_wait_budget;
 
 // Waits for the phase with the given parity to complete.  Returns false if the budget ran out or
