@@ -35,8 +35,8 @@
 // TMEM columns: two step buffers [0,64) and [64,128), each holding S^T, then P^T as bf16 over its
 // first 32 columns, then dQ^T; dP^T [128,192) (dS^T as bf16 over its first 32); K_j as bf16 [192,192+D/2)
 // (the A operand of S^T: it stays resident, so S^T reads only Q_i from shared memory); dV [256,256+D),
-// dK [256+D,256+2D).  Shared-memory bandwidth is what bounds this kernel, so every operand that can
-// come from tensor memory does.
+// dK [256+D,256+2D).  Three of the five products have N = 64 (the query step), and those MMAs set
+// this kernel's pace.
 
 #include <cuda_bf16.h>
 #include <math.h>
@@ -477,45 +477,57 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 }
 
 // -D_i = -(dO_i . O_i) and -LSE2_i = -LSE_i log2(e) into [head][Npad] arrays (pad rows: 0 and -inf);
-// zeroes the fp32 dQ accumulator.  One warp per (padded) row, grid-stride.
+// zeroes the fp32 dQ accumulator.  D/8 threads share a row (16-byte loads of O and dO), each warp takes
+// 2 * 32 / (D/8) rows per pass, so enough bytes are in flight to stream at HBM speed.
+template <int D>
 __global__ void bwd_prep_kernel(const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dout,
                                 const float* __restrict__ lse, float* __restrict__ row_d, float* __restrict__ lse2,
-                                float* __restrict__ dq_acc, int N, int Npad, int d, int64_t heads) {
+                                float* __restrict__ dq_acc, int N, int Npad, int64_t heads) {
+    constexpr int kTpr = D / 8;          // threads per row
+    constexpr int kRpw = 32 / kTpr;      // rows per warp and pass
     const int lane = threadIdx.x & 31;
-    const int64_t warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int sub = lane / kTpr, part = lane % kTpr;
+    const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t warp_id = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     const int64_t rows = heads * Npad;
-    for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < rows; w += warps) {
-        const int64_t h = w / Npad;
-        const int r = (int)(w - h * Npad);
-        if (r >= N) {
-            if (lane == 0) {
-                row_d[w] = 0.f;
-                lse2[w] = -INFINITY;
-            }
-            continue;
-        }
-        const size_t src = ((size_t)h * N + r) * d;
-        float acc = 0.f;
-        for (int c = lane * 4; c < d; c += 128) {
-            const uint2 a = *reinterpret_cast<const uint2*>(o + src + c);
-            const uint2 b = *reinterpret_cast<const uint2*>(dout + src + c);
-            const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
-            const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&b);
+    for (int64_t base = warp_id * 2 * kRpw; base < rows; base += nwarps * 2 * kRpw) {
+        float acc[2];
+        int64_t w[2];
+        bool valid[2];
 #pragma unroll
-            for (int t = 0; t < 2; ++t) {
-                const float2 fa = __bfloat1622float2(a2[t]);
-                const float2 fb = __bfloat1622float2(b2[t]);
-                acc = fmaf(fa.x, fb.x, acc);
-                acc = fmaf(fa.y, fb.y, acc);
+        for (int u = 0; u < 2; ++u) {
+            w[u] = base + u * kRpw + sub;
+            const int64_t h = w[u] / Npad;
+            const int r = (int)(w[u] - h * Npad);
+            valid[u] = w[u] < rows && r < N;
+            acc[u] = 0.f;
+            if (valid[u]) {
+                const size_t off = ((size_t)h * N + r) * D + part * 8;
+                const uint4 a = *reinterpret_cast<const uint4*>(o + off);
+                const uint4 g = *reinterpret_cast<const uint4*>(dout + off);
+                const __nv_bfloat162* a2 = reinterpret_cast<const __nv_bfloat162*>(&a);
+                const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(&g);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 fa = __bfloat1622float2(a2[t]), fg = __bfloat1622float2(g2[t]);
+                    acc[u] = fmaf(fa.x, fg.x, fmaf(fa.y, fg.y, acc[u]));
+                }
             }
         }
-        for (int off = 16; off; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
-            row_d[w] = -acc;
-            lse2[w] = -lse[(size_t)h * N + r] * 1.4426950408889634f;
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+#pragma unroll
+            for (int off = kTpr / 2; off; off >>= 1) acc[u] += __shfl_xor_sync(0xffffffffu, acc[u], off);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (part != 0 || w[u] >= rows) continue;
+            const int64_t h = w[u] / Npad;
+            const int r = (int)(w[u] - h * Npad);
+            row_d[w[u]] = valid[u] ? -acc[u] : 0.f;
+            lse2[w[u]] = valid[u] ? -lse[(size_t)h * N + r] * 1.4426950408889634f : -INFINITY;
         }
     }
-    const int64_t n4 = heads * (int64_t)N * d / 4;
+    const int64_t n4 = heads * (int64_t)N * D / 4;
     float4* z = reinterpret_cast<float4*>(dq_acc);
     for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < n4; idx += (int64_t)gridDim.x * blockDim.x)
         z[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -556,8 +568,8 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     float* lse2 = (float*)(ws + w.lse2);
     const int Npad = bwd_padded_rows(s.N);
     const int blocks = sm_count() * 4;
-    bwd_prep_kernel<<<blocks, 256, 0, st>>>((const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, lse, row_d, lse2,
-                                            dq_acc, s.N, Npad, s.d, s.heads());
+    bwd_prep_kernel<D><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, lse, row_d,
+                                               lse2, dq_acc, s.N, Npad, s.heads());
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 
