@@ -60,6 +60,18 @@ WaitPolicy wait_policy() {
     return WaitPolicy{4000000000LL, 0};                       // ~2 s: no legitimate wait comes near it
 }
 
+int device_sm_count() {
+    static int counts[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+    if (!counts[dev]) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        counts[dev] = n;
+    }
+    return counts[dev];
+}
+
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Common checks of every entry point; returns FA_OK or the error (message already recorded).

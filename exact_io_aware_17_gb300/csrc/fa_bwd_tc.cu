@@ -546,17 +546,6 @@ __global__ void bwd_dq_convert_kernel(const float* __restrict__ dq_acc, __nv_bfl
     }
 }
 
-int sm_count() {
-    static int n = 0;
-    if (!n) {
-        int dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        if (n <= 0) n = 148;
-    }
-    return n;
-}
-
 template <int D>
 cudaError_t launch(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
                    void* dq, void* dk, void* dv, const Shape& s, float scale, void* workspace, cudaStream_t st) {
@@ -567,7 +556,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     float* row_d = (float*)(ws + w.row_d);
     float* lse2 = (float*)(ws + w.lse2);
     const int Npad = bwd_padded_rows(s.N);
-    const int blocks = sm_count() * 4;
+    const int blocks = device_sm_count() * 4;
     bwd_prep_kernel<D><<<blocks, 256, 0, st>>>((const __nv_bfloat16*)o, (const __nv_bfloat16*)dout, lse, row_d,
                                                lse2, dq_acc, s.N, Npad, s.heads());
     cudaError_t e = cudaGetLastError();

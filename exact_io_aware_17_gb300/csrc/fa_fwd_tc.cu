@@ -25,6 +25,13 @@
 // lane), warp 8 issues TMA loads, warp 9 allocates TMEM and issues the MMAs.  While one warpgroup
 // exponentiates its S tile the tensor cores run the other tile's MMAs.
 //
+// Work: a CTA takes a pair of adjacent 128-row tiles of one head (a head-major 1-D grid).  When the
+// pairs do not fill the GPU's last wave, those last pairs run as 2-CTA clusters instead: each CTA of a
+// cluster streams half of the K/V blocks, rank 1 hands its unnormalised O, m and l to rank 0 through
+// distributed shared memory, and rank 0 merges the halves,
+//     m = max(m0, m1),  l = 2^(m0-m) l0 + 2^(m1-m) l1,  O = (2^(m0-m) O0 + 2^(m1-m) O1) / l,
+// the same exp-sum factorisation as the online rescale.  The last wave then takes half as long.
+//
 // TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
 
 #include <cuda_bf16.h>
@@ -81,7 +88,7 @@ struct FwdCfg {
 
 template <int D>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint8_t* smem,
-                         FwdBarriers* bars, int head, int q0, int T, int starve) {
+                         FwdBarriers* bars, int head, int q0, int kv0, int T, int starve) {
     using C = FwdCfg<D>;
     volatile int* abort_flag = &bars->abort;
     const uint64_t pol_kv = policy_evict_last();
@@ -100,12 +107,12 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         if (j >= C::kStages && !mbar_wait(&bars->kv_empty[s], ((j / C::kStages) - 1) & 1, abort_flag)) break;
         mbar_expect_tx(&bars->k_full[s], C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem + C::kOffK + s * C::kKVBytes + c * C::kChunkKV, tm_k, &bars->k_full[s], c * 64, j * BN,
-                        head, pol_kv);
+            tma_load_3d(smem + C::kOffK + s * C::kKVBytes + c * C::kChunkKV, tm_k, &bars->k_full[s], c * 64,
+                        (kv0 + j) * BN, head, pol_kv);
         mbar_expect_tx(&bars->v_full[s], C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem + C::kOffV + s * C::kKVBytes + c * C::kChunkKV, tm_v, &bars->v_full[s], c * 64, j * BN,
-                        head, pol_kv);
+            tma_load_3d(smem + C::kOffV + s * C::kKVBytes + c * C::kChunkKV, tm_v, &bars->v_full[s], c * 64,
+                        (kv0 + j) * BN, head, pol_kv);
         issued = j + 1;
     }
     // Every load issued must have landed before the CTA may exit (only matters after an abort).
@@ -189,7 +196,8 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
 
 template <int D, bool kStepNorm>
 __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat16* __restrict__ o,
-                           float* __restrict__ lse, int head, int q0, int N, int T, float scale_log2) {
+                           float* __restrict__ lse, int head, int q0, int N, int kv0, int T, int T_all,
+                           float scale_log2, float* ml_out) {
     using C = FwdCfg<D>;
     volatile int* abort_flag = &bars->abort;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -197,7 +205,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + C::col_s(t) + lane_off;
     const uint32_t tO = tmem + C::col_o(t) + lane_off;
-    const int tail = N - (T - 1) * BN;  // valid keys in the last block (1..BN)
+    const int tail = N - (T_all - 1) * BN;  // valid keys in the head's last block (1..BN)
 
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
@@ -208,7 +216,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, r[q]);
         tmem_ld_wait();
-        if (j == T - 1 && tail < BN) {
+        if (kv0 + j == T_all - 1 && tail < BN) {
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -325,6 +333,11 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
     if (!ok) return;
     if (!warp_wait(&bars->o_full[t], 0, abort_flag)) return;
     tc_fence_after();
+    if (ml_out) {  // one half of a split pair: O stays in TMEM, m and l go to shared memory for the merge
+        ml_out[t * BM + quarter * 32 + lane] = m_run;
+        ml_out[2 * BM + t * BM + quarter * 32 + lane] = l_run;
+        return;
+    }
 
     const int row = q0 + t * BM + quarter * 32 + lane;
     const float inv_l = kStepNorm ? 1.f : 1.f / l_run;
@@ -347,20 +360,92 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
     if (row < N) lse[(size_t)head * N + row] = (m_run + log2f(l_run)) * 0.69314718055994531f;
 }
 
+// Rank 1 of a split pair: this thread's row of O (from TMEM), m and l into rank 0's shared memory
+// (O column-major by row so that a warp's stores land in consecutive words).
+template <int D>
+__device__ void split_send(uint8_t* smem, uint32_t tmem, int t) {
+    using C = FwdCfg<D>;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t o_peer = mapa_shared(smem_u32(smem + C::kOffK), 0);
+    const uint32_t ml_peer = mapa_shared(smem_u32(smem + C::kOffQ), 0);
+    const float* ml_own = reinterpret_cast<const float*>(smem + C::kOffQ + 4096);
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t x[32];
+        tmem_ld32(tmem + C::col_o(t) + lane_off + q * 32, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            st_cluster_f32(o_peer + (uint32_t)(((t * D + q * 32 + c) * BM + r) * 4), __uint_as_float(x[c]));
+    }
+    st_cluster_f32(ml_peer + (uint32_t)((t * BM + r) * 4), ml_own[t * BM + r]);
+    st_cluster_f32(ml_peer + (uint32_t)((2 * BM + t * BM + r) * 4), ml_own[2 * BM + t * BM + r]);
+}
+
+// Rank 0 of a split pair: merges its own half (TMEM, m and l in shared memory) with the received one and
+// writes this thread's row of O and LSE.
+template <int D>
+__device__ void split_merge(uint8_t* smem, uint32_t tmem, int t, __nv_bfloat16* __restrict__ o,
+                            float* __restrict__ lse, int head, int q0, int N) {
+    using C = FwdCfg<D>;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const float* opart = reinterpret_cast<const float*>(smem + C::kOffK);
+    const float* ml_peer = reinterpret_cast<const float*>(smem + C::kOffQ);
+    const float* ml_own = reinterpret_cast<const float*>(smem + C::kOffQ + 4096);
+    const float m0 = ml_own[t * BM + r], l0 = ml_own[2 * BM + t * BM + r];
+    const float m1 = ml_peer[t * BM + r], l1 = ml_peer[2 * BM + t * BM + r];
+    const float m = fmaxf(m0, m1);
+    const float a0 = ex2(m0 - m), a1 = ex2(m1 - m);
+    const float l = a0 * l0 + a1 * l1;
+    const float inv = 1.f / l;
+    const int row = q0 + t * BM + r;
+    const size_t base = ((size_t)head * N + row) * D;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t x[32];
+        tmem_ld32(tmem + C::col_o(t) + lane_off + q * 32, x);
+        tmem_ld_wait();
+        uint32_t pk[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const int col = q * 32 + 2 * c;
+            const float v0 = (a0 * __uint_as_float(x[2 * c]) + a1 * opart[(t * D + col) * BM + r]) * inv;
+            const float v1 = (a0 * __uint_as_float(x[2 * c + 1]) + a1 * opart[(t * D + col + 1) * BM + r]) * inv;
+            pk[c] = pack_bf16(v0, v1);
+        }
+        if (row < N) {
+            uint4* dst = reinterpret_cast<uint4*>(o + base + q * 32);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+    }
+    if (row < N) lse[(size_t)head * N + row] = (m + log2f(l)) * 0.69314718055994531f;
+}
+
 template <int D, bool kStepNorm>
 __global__ void __launch_bounds__(kThreads, 1)
 fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-              int N, int blocks_per_head, float scale_log2, long long wait_budget, int starve) {
+              int N, int blocks_per_head, int pair_base, int split, float scale_log2, long long wait_budget,
+              int starve) {
     using C = FwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
     FwdBarriers* bars = reinterpret_cast<FwdBarriers*>(smem + C::kOffBar);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    // 1-D grid, head-major: the CTAs of one head run together and share its K/V through L2.
-    const int head = blockIdx.x / blocks_per_head;
-    const int q0 = (blockIdx.x % blocks_per_head) * 2 * BM;
-    const int T = (N + BN - 1) / BN;
+    // 1-D grid, head-major: the CTAs of one head run together and share its K/V through L2.  With
+    // split != 0 two consecutive CTAs (one cluster) share pair pair_base + blockIdx.x / 2.
+    const int pair = pair_base + (split ? (int)blockIdx.x / 2 : (int)blockIdx.x);
+    const int head = pair / blocks_per_head;
+    const int q0 = (pair % blocks_per_head) * 2 * BM;
+    const int T_all = (N + BN - 1) / BN;
+    const uint32_t rank = split ? cluster_ctarank() : 0;
+    const int kv0 = split ? (int)rank * (T_all / 2) : 0;
+    const int T = split ? (rank ? T_all - T_all / 2 : T_all / 2) : T_all;
 
     if (threadIdx.x == 0) {
         s_wait_budget = wait_budget;
@@ -394,15 +479,27 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == kTmaWarp) {
-        if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, smem, bars, head, q0, T, starve);
+        if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, smem, bars, head, q0, kv0, T, starve);
     } else if (warp == kMmaWarp) {
         if (lane == 0) mma_issuer<D>(smem, bars, tmem, T);
     } else {
-        softmax_wg<D, kStepNorm>(bars, tmem, warp / 4, o, lse, head, q0, N, T, scale_log2);
+        softmax_wg<D, kStepNorm>(bars, tmem, warp / 4, o, lse, head, q0, N, kv0, T, T_all, scale_log2,
+                                 split ? reinterpret_cast<float*>(smem + C::kOffQ + 4096) : nullptr);
     }
 
     tc_fence_before();
     __syncthreads();
+    if (split) {
+        // Every thread of both CTAs reaches both cluster barriers: all waits before them are bounded.
+        cluster_sync();  // both halves done: rank 0's K/V and Q buffers are free to receive
+        tc_fence_after();
+        const bool both_ok = !bars->abort;
+        if (rank == 1 && warp < 8 && both_ok) split_send<D>(smem, tmem, warp / 4);
+        cluster_sync();  // rank 1's stores are visible to rank 0
+        if (rank == 0 && warp < 8 && both_ok) split_merge<D>(smem, tmem, warp / 4, o, lse, head, q0, N);
+        tc_fence_before();
+        __syncthreads();
+    }
     if (warp == kMmaWarp) {
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
@@ -423,11 +520,38 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
     if (e != cudaSuccess) return e;
     const int bph = (s.N + 2 * BM - 1) / (2 * BM);
     if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
-    const unsigned grid = (unsigned)(bph * s.heads());
+    const long long pairs = (long long)bph * s.heads();
+    // Whole waves of pair CTAs; a last partial wave runs as split pairs (2-CTA clusters) when it fits.
+    const long long sms = device_sm_count();
+    const long long full = (pairs / sms) * sms, rest = pairs - full;
+    const int T_all = (s.N + BN - 1) / BN;
+    const bool split_tail = !kStepNorm && T_all >= 2 && rest > 0 && 2 * rest <= sms;
+    const unsigned grid = (unsigned)(split_tail ? full : pairs);
     const float scale_log2 = scale * 1.4426950408889634f;
     const WaitPolicy wp = wait_policy();
-    fwd_tc_kernel<D, kStepNorm><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, (__nv_bfloat16*)o, lse, s.N, bph, scale_log2,
-                                                            wp.budget_cycles, wp.starve);
+    auto* out = (__nv_bfloat16*)o;
+    if (grid > 0) {
+        fwd_tc_kernel<D, kStepNorm><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, out, lse, s.N, bph, 0, 0,
+                                                                           scale_log2, wp.budget_cycles, wp.starve);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (split_tail) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(2 * rest));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, kStepNorm>, tq, tk, tv, out, lse, s.N, bph, (int)full, 2,
+                               scale_log2, wp.budget_cycles, wp.starve);
+        if (e != cudaSuccess) return e;
+    }
     return cudaGetLastError();
 }
 

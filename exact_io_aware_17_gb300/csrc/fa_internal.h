@@ -41,6 +41,9 @@ struct WaitPolicy {
 };
 WaitPolicy wait_policy();
 
+// Multiprocessor count of the current device (cached per device).
+int device_sm_count();
+
 // Encodes a TMA descriptor for a bf16 [heads, N, d] array (d innermost) with boxes of 64 columns x
 // `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows);

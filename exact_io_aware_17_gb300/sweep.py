@@ -5,6 +5,10 @@
 Each shape runs B=1 with H chosen so that B*H*N = 131072 rows (the headline workload's size), seeded
 N(0,1) bf16 inputs, L2 flushed between timed calls, median of --iters CUDA-event timings.  Prints one
 JSON line per shape with TFLOP/s and the fraction of the measured bf16 peak.
+
+    python -m exact_io_aware_17_gb300.sweep --workload bf16-fwd-B1-H8-N32768-d128-q4
+
+times the forward (and the backward when the workload has one) on a named workload's own inputs.
 """
 import argparse
 import json
@@ -50,11 +54,35 @@ def main():
     ap.add_argument("--d", type=int, nargs="+", default=[64, 128])
     ap.add_argument("--rows", type=int, default=131072, help="B*H*N of every shape")
     ap.add_argument("--iters", type=int, default=10)
+    ap.add_argument("--workload", nargs="+", default=None, choices=sorted(fa_inputs.WORKLOADS),
+                    help="time named workloads (their own shapes and inputs) instead of the N x d grid")
     ap.add_argument("--stepnorm", action="store_true",
                     help="also time fa_fwd_stepnorm (the per-step normalised update rule)")
     a = ap.parse_args()
     peak, src = _peak()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    if a.workload:
+        for name in a.workload:
+            w = fa_inputs.WORKLOADS[name]
+            if w.dtype != "bf16":
+                continue
+            inp = fa_inputs.workload_inputs(w, with_grad=w.backward)
+            t = {n: x.cuda() for n, x in inp.items()}
+            o, lse = fa.fa_fwd(t["q"], t["k"], t["v"], w.scale)
+            tf = _time(lambda: fa.fa_fwd(t["q"], t["k"], t["v"], w.scale, o, lse), flush, a.iters)
+            line = {"workload": name, "fwd_ms": tf, "fwd_tflops": w.fwd_flops() / tf / 1e9,
+                    "fwd_frac": w.fwd_flops() / tf / 1e9 / peak, "peak_tflops": peak, "peak_source": src}
+            if w.backward:
+                dq, dk, dv = (torch.empty_like(t["q"]) for _ in range(3))
+                ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device="cuda")
+                tb = _time(lambda: fa.fa_bwd(t["q"], t["k"], t["v"], o, t["do"], lse, w.scale, dq, dk, dv, ws),
+                           flush, a.iters)
+                line.update(bwd_ms=tb, bwd_tflops=w.bwd_flops() / tb / 1e9, bwd_frac=w.bwd_flops() / tb / 1e9 / peak)
+            fa.fa_check_status()
+            print(json.dumps(line), flush=True)
+            del t, o, lse
+            torch.cuda.empty_cache()
+        return
     for d in a.d:
         for N in a.N:
             H = max(1, a.rows // N)
