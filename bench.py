@@ -232,6 +232,7 @@ def run_ours(args, w):
 
     e2e_ms, h2d, d2h = _e2e(fa, w, inp_cpu, dev, args.steps)
     e2e_ms = max_over_ranks(e2e_ms, dev)
+    launches = _count_launches(step)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -243,7 +244,8 @@ def run_ours(args, w):
         "fwd_bwd_frac_of_peak": value / world / peak,
         "wall_s_timed_region": wall,
         "clocks": clk,
-        "gpu_launches": args.steps * LAUNCHES_PER_STEP,
+        "gpu_launches": args.steps * launches["per_step"],
+        "gpu_launches_per_step": launches,
         "e2e": {"value": (w.fwd_flops() + w.bwd_flops()) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q,k,v,dO copied in and o,lse,dq,dk,dv copied out every step, through the "
@@ -318,14 +320,38 @@ def _e2e(fa, w, inp_cpu, dev, steps):
     return start.elapsed_time(end) / steps, 4 * elt, 4 * elt + B * H * N * 4
 
 
-# Kernels launched per step: the forward kernel, and the backward's row-term, main and dQ kernels.
-LAUNCHES_PER_STEP = 4
+# Kernels launched per step when the profiler interface is unavailable: the forward's full waves and
+# its 2-CTA-cluster tail wave, and the backward's row-term, main and dQ kernels.
+LAUNCHES_PER_STEP_SCHEDULE = 5
+# Kernel names of libfa.so (they appear in both demangled and mangled profiler names).
+OUR_KERNELS = ("fwd_tc_kernel", "bwd_prep_kernel", "bwd_tc_kernel", "bwd_dq_convert_kernel", "fwd_simt_kernel")
+
+
+def _count_launches(step):
+    """Kernels of libfa.so launched by one (untimed) step, counted through the CUDA profiler interface
+    after every timed region has finished."""
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step()
+            torch.cuda.synchronize()
+        names = [e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA]
+        mine = [n for n in names if any(k in n for k in OUR_KERNELS)]
+        ours = sorted({k for n in mine for k in OUR_KERNELS if k in n})
+        count = len(mine)
+        if count:
+            return {"per_step": count, "counted_by": "torch.profiler (CUPTI), one untimed step",
+                    "kernels": ours}
+    except Exception as e:                                   # profiler interface missing on this host
+        return {"per_step": LAUNCHES_PER_STEP_SCHEDULE, "counted_by": f"schedule (profiler failed: {e})"}
+    return {"per_step": LAUNCHES_PER_STEP_SCHEDULE, "counted_by": "schedule (profiler saw no kernels)"}
 
 
 # DRAM bytes per launch of the dominant kernel at the bench workload, from one ncu capture of the
 # kernel as it is built now (profiles/dram_per_launch_bench_B1-H16-N8192-d128.md).  Set to None whenever
 # the kernel changes until it is measured again.
-TRAFFIC_BYTES = {("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): 202448640 + 82996480}
+TRAFFIC_BYTES = {("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): None}
 
 
 def _roofline(w, fwd_ms, bwd_ms, peaks):

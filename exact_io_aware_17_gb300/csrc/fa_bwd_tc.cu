@@ -7,36 +7,41 @@
 //     dK = scale dS^T Q,  dQ = scale dS K.
 //
 // Three kernels per call:
-//   bwd_prep_kernel   -D_i and -LSE_i * log2(e) per query row (padded to a multiple of 64 rows per head;
+//   bwd_prep_kernel   -D_i and -LSE_i * log2(e) per query row (padded to a multiple of 128 rows per head;
 //                     pad rows get 0 and -inf so they contribute nothing), and zeroes the fp32 dQ
 //                     accumulator.  Negated so that the main kernel applies them with packed-pair adds.
 //   bwd_tc_kernel     one CTA per (head, block of 128 keys).  K_j, V_j stay in shared memory; the CTA
-//                     walks every block of 64 queries i:
-//                         S^T  = K_j Q_i^T            K_j as bf16 from tensor memory; fp32 result,
-//                                                     double buffered
+//                     walks every block of 128 queries i:
+//                         S^T  = K_j Q_i^T              fp32 in tensor memory
 //                         dP^T = V_j dO_i^T
 //                         P^T  = exp2(S^T scale log2e - LSE2_i)    thread = key row; packed fp32
-//                                                     pairs (f32x2) for the element-wise work
+//                                                       pairs (f32x2) for the element-wise work
 //                         dS^T = P^T o (dP^T - D_i)
-//                         dV_j += P^T dO_i            P^T as bf16 from tensor memory
-//                         dK_j += dS^T Q_i            dS^T as bf16 from tensor memory
-//                         dQ_i^T = K_j^T dS^T         dS^T as bf16 from shared memory, into the
-//                                                     S^T buffer of the step (free once dV used P^T)
+//                         dV_j += P^T dO_i              P^T as bf16 from tensor memory
+//                         dK_j += dS^T Q_i              dS^T as bf16 from tensor memory
+//                         dQ_i^T = K_j^T dS^T           dS^T as bf16 from shared memory, into the
+//                                                       columns of dP^T (free once dK used dS^T)
 //                     and adds dQ_i into the fp32 accumulator with bulk reduce-add copies.
 //   bwd_dq_convert    dQ = bf16(scale * accumulator).
 //
-// Warp roles of bwd_tc_kernel (320 threads): warps 0-3 own the 128 key rows (softmax gradient and the
-// dK/dV epilogue), warps 4-7 drain dQ^T (thread = head-dimension index) into the accumulator,
-// warp 8 issues TMA loads, warp 9 allocates tensor memory and issues the MMAs.
+// Every product is 128 x 128 x 128 (M = 128 keys or head dimensions, N = 128 queries or head
+// dimensions): N = 128 is the narrowest tcgen05 shape that runs at the full rate, which 64-query steps
+// (three of five products at N = 64) did not reach.  Tensor memory then holds exactly S^T, dP^T, dV and
+// dK (4 x 128 columns at d = 128), with dQ^T reusing the columns of dP^T.  S^T of the next step is issued
+// right behind dQ^T, so moving dQ^T out of tensor memory overlaps the next S^T.
+//
+// Warp roles (320 threads): warps 0-3 and 4-7 are two warpgroups that own the same 128 key rows
+// (tensor-memory lanes) and split each step's queries, 64 each: they form P^T and dS^T for their half,
+// then move their half of dQ_i^T out of tensor memory (thread = head-dimension index) and issue its
+// reduce-add, and at the end write dV (warps 0-3) and dK (warps 4-7).  Warp 8 issues TMA loads, warp 9
+// allocates tensor memory and issues the MMAs.
+//
+// Shared memory (d = 128: 226 KB) has one dQ staging buffer: the first half's dQ rows are staged in the
+// Q tile of the step (no longer read once dK has been formed), which the TMA thread adds into the
+// accumulator and then reloads; the second half's rows have a buffer of their own.
 //
 // For d = 64 the dQ^T product still uses M = 128: the A operand's second 64-row half points at a
 // zeroed shared-memory block, and the rows it produces are ignored.
-//
-// TMEM columns: two step buffers [0,64) and [64,128), each holding S^T, then P^T as bf16 over its
-// first 32 columns, then dQ^T; dP^T [128,192) (dS^T as bf16 over its first 32); K_j as bf16 [192,192+D/2)
-// (the A operand of S^T: it stays resident, so S^T reads only Q_i from shared memory); dV [256,256+D),
-// dK [256+D,256+2D).  Three of the five products have N = 64 (the query step), and those MMAs set
-// this kernel's pace.
 
 #include <cuda_bf16.h>
 #include <math.h>
@@ -52,33 +57,37 @@ using namespace ptx;
 __device__ int g_bwd_status;
 
 constexpr int BK = 128;  // keys per CTA
-constexpr int BQ = 64;   // queries per step
+constexpr int BQ = 128;  // queries per step
+constexpr int HQ = 64;   // queries per warpgroup half of a step
 constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kStages = 3;
+constexpr int kQStages = 2;
 
 struct BwdBarriers {
     uint64_t kv_full;
-    uint64_t qdo_full[kStages];
-    uint64_t qdo_empty[kStages];
-    uint64_t s_full[2];
+    uint64_t q_full[kQStages];     // Q tile + LSE2 and -D rows of a step
+    uint64_t staged_q[kQStages];   // the first half's dQ rows are staged in this Q tile
+    uint64_t do_full[2];
+    uint64_t do_empty[2];
+    uint64_t s_full;
     uint64_t dp_full;
-    uint64_t p_ready;
-    uint64_t ds_ready;
+    uint64_t p_ready[2];
+    uint64_t ds_ready[2];
     uint64_t dq_full;
     uint64_t dq_empty;
-    uint64_t ds_free[2];
+    uint64_t staged_b;             // the second half's dQ rows are in their staging buffer
+    uint64_t stage_b_free;         // ... and their reduce has read them
     uint64_t dkdv_full;
-    uint64_t ka_ready;
     uint64_t mma_done;
     uint32_t tmem_base;
-    int abort;
+    WaitCtl wait;
 };
 
 template <int D>
 struct BwdCfg {
     static constexpr int kChunks = D / 64;
+    static constexpr int kDOStages = D == 64 ? 2 : 1;
     static constexpr uint32_t kChunkK = BK * 128;          // one 64-column chunk of a K or V tile
     static constexpr uint32_t kChunkQ = BQ * 128;          // one 64-column chunk of a Q or dO tile
     static constexpr uint32_t kKBytes = BK * D * 2;
@@ -88,79 +97,116 @@ struct BwdCfg {
     static constexpr uint32_t kZeroBytes = (D == 64) ? kChunkK : 0;
     static constexpr uint32_t kOffV = kOffZero + kZeroBytes;
     static constexpr uint32_t kOffQ = kOffV + kKBytes;
-    static constexpr uint32_t kOffDO = kOffQ + kStages * kQBytes;
-    static constexpr uint32_t kDSBytes = BK * BQ * 2;      // dS^T tile: 128 key rows x 128 bytes
-    static constexpr uint32_t kOffDS = kOffDO + kStages * kQBytes;
-    static constexpr uint32_t kDQBytes = BQ * D * 4;       // fp32 dQ staging [BQ][D]
-    static constexpr uint32_t kOffDQ = kOffDS + 2 * kDSBytes;
-    static constexpr uint32_t kRowBytes = BQ * 4;          // LSE2 or D of one query block
-    static constexpr uint32_t kOffRows = kOffDQ + kDQBytes; // [stage][2][BQ] floats
-    static constexpr uint32_t kOffBar = kOffRows + kStages * 2 * kRowBytes;
-    static constexpr uint32_t kSmemBytes = kOffBar + sizeof(BwdBarriers) + 1024;
-    static constexpr uint32_t kColDP = 128, kColKA = 192, kColDV = 256, kColDK = 256 + D;
+    static constexpr uint32_t kOffDO = kOffQ + kQStages * kQBytes;
+    static constexpr uint32_t kDSChunk = BK * 128;         // dS^T of one half: 128 key rows x 64 queries
+    static constexpr uint32_t kOffDS = kOffDO + kDOStages * kQBytes;
+    static constexpr uint32_t kHalfDQBytes = HQ * D * 4;   // fp32 dQ rows [HQ][D] of one half
+    static constexpr uint32_t kOffStageB = kOffDS + 2 * kDSChunk;   // the second half's dQ rows
+    static constexpr uint32_t kRowBytes = BQ * 4;          // LSE2 or -D of one query block
+    static constexpr uint32_t kOffRows = kOffStageB + kHalfDQBytes;  // [q stage][LSE2 | -D][BQ] floats
+    static constexpr uint32_t kOffBar = kOffRows + kQStages * 2 * kRowBytes;
+    static constexpr uint32_t kSmemNeed = kOffBar + sizeof(BwdBarriers);
+    // Room to align the region to 1024 bytes if the dynamic shared memory does not start aligned (it
+    // does when the kernel has no static shared memory, which is the case here).
+    static constexpr uint32_t kAlignSlack = kSmemNeed + 1024 <= 232448 ? 1024 : 232448 - kSmemNeed;
+    static constexpr uint32_t kSmemBytes = kSmemNeed + kAlignSlack;
+    static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
-    __host__ __device__ static constexpr uint32_t col_s(int b) { return (uint32_t)b * 64; }
+    static_assert(kHalfDQBytes == kQBytes, "the first half's dQ rows are staged in the step's Q tile");
+    static_assert(kSmemNeed <= 232448, "shared memory per CTA");
 };
+
+// Query block visited at step i by a CTA whose walk starts at block `rot`.
+__device__ __forceinline__ int qblock(int i, int rot, int Tq) {
+    const int b = i + rot % Tq;
+    return b < Tq ? b : b - Tq;
+}
 
 template <int D>
 __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                             const CUtensorMap* tm_do, const float* lse2, const float* row_d, uint8_t* smem,
-                             BwdBarriers* bars, int head, int k0, int Tq, int Npad) {
+                             const CUtensorMap* tm_do, const float* lse2, const float* row_d,
+                             float* __restrict__ dq_acc, uint8_t* smem, BwdBarriers* bars, int head, int k0, int N,
+                             int Tq, int Npad, int rot) {
     using C = BwdCfg<D>;
-    volatile int* abort_flag = &bars->abort;
+    WaitCtl* wc = &bars->wait;
     const uint64_t pol_keep = policy_evict_last();
     mbar_expect_tx(&bars->kv_full, 2 * C::kKBytes);
     for (int c = 0; c < C::kChunks; ++c) {
         tma_load_3d(smem + C::kOffK + c * C::kChunkK, tm_k, &bars->kv_full, c * 64, k0, head, pol_keep);
         tma_load_3d(smem + C::kOffV + c * C::kChunkK, tm_v, &bars->kv_full, c * 64, k0, head, pol_keep);
     }
-    int issued = 0;
-    for (int i = 0; i < Tq; ++i) {
-        const int s = i % kStages;
-        if (i >= kStages && !mbar_wait(&bars->qdo_empty[s], ((i / kStages) - 1) & 1, abort_flag)) break;
-        uint64_t* bar = &bars->qdo_full[s];
-        mbar_expect_tx(bar, 2 * C::kQBytes + 2 * C::kRowBytes);
-        for (int c = 0; c < C::kChunks; ++c) {
-            tma_load_3d(smem + C::kOffQ + s * C::kQBytes + c * C::kChunkQ, tm_q, bar, c * 64, i * BQ, head, pol_keep);
-            tma_load_3d(smem + C::kOffDO + s * C::kQBytes + c * C::kChunkQ, tm_do, bar, c * 64, i * BQ, head,
-                        pol_keep);
+    // The first half's dQ rows of step j are staged in Q tile j % kQStages.  This thread adds them into
+    // the accumulator and reloads the tile once the reduce has read it, so it owns the tile's whole cycle.
+    auto reduce_first_half = [&](int j) -> bool {
+        const int s = j % kQStages;
+        if (!mbar_wait(&bars->staged_q[s], (j / kQStages) & 1, wc)) return false;
+        const int q0 = qblock(j, rot, Tq) * BQ;
+        const int rows = min(HQ, N - q0);
+        if (rows > 0) {
+            bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, smem + C::kOffQ + s * C::kQBytes,
+                                (uint32_t)(rows * D * 4));
+            bulk_commit_group();
         }
+        return true;
+    };
+    int q_issued = 0, do_issued = 0;
+    bool ok = true;
+    for (int i = 0; i < Tq && ok; ++i) {
+        const int s = i % kQStages;
+        if (i >= kQStages) {
+            if (!(ok = reduce_first_half(i - kQStages))) break;
+            bulk_wait_group_read<0>();
+        }
+        const int qb = qblock(i, rot, Tq);
+        uint64_t* bar = &bars->q_full[s];
+        mbar_expect_tx(bar, C::kQBytes + 2 * C::kRowBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffQ + s * C::kQBytes + c * C::kChunkQ, tm_q, bar, c * 64, qb * BQ, head, pol_keep);
         float* rows = reinterpret_cast<float*>(smem + C::kOffRows) + s * 2 * BQ;
-        const size_t r0 = (size_t)head * Npad + (size_t)i * BQ;
+        const size_t r0 = (size_t)head * Npad + (size_t)qb * BQ;
         bulk_load(rows, lse2 + r0, C::kRowBytes, bar);
         bulk_load(rows + BQ, row_d + r0, C::kRowBytes, bar);
-        issued = i + 1;
+        q_issued = i + 1;
+
+        const int t = i % C::kDOStages;
+        if (i >= C::kDOStages &&
+            !(ok = mbar_wait(&bars->do_empty[t], ((i / C::kDOStages) - 1) & 1, wc)))
+            break;
+        mbar_expect_tx(&bars->do_full[t], C::kQBytes);
+        for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(smem + C::kOffDO + t * C::kQBytes + c * C::kChunkQ, tm_do, &bars->do_full[t], c * 64, qb * BQ,
+                        head, pol_keep);
+        do_issued = i + 1;
     }
-    drain_wait(&bars->kv_full, 0);
-    for (int i = (issued > kStages ? issued - kStages : 0); i < issued; ++i)
-        drain_wait(&bars->qdo_full[i % kStages], (i / kStages) & 1);
+    for (int j = (Tq > kQStages ? Tq - kQStages : 0); ok && j < Tq; ++j) ok = reduce_first_half(j);
+    bulk_wait_group<0>();
+    // Copies still in flight must land before the CTA can exit.
+    drain_wait(&bars->kv_full, 0, wc);
+    for (int i = (q_issued > kQStages ? q_issued - kQStages : 0); i < q_issued; ++i)
+        drain_wait(&bars->q_full[i % kQStages], (i / kQStages) & 1, wc);
+    for (int i = (do_issued > C::kDOStages ? do_issued - C::kDOStages : 0); i < do_issued; ++i)
+        drain_wait(&bars->do_full[i % C::kDOStages], (i / C::kDOStages) & 1, wc);
 }
 
 template <int D>
 __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq) {
     using C = BwdCfg<D>;
-    volatile int* abort_flag = &bars->abort;
-    constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, 0, 0);   // S^T (A from TMEM), dP^T (A K-major); B K-major [q][d]
+    WaitCtl* wc = &bars->wait;
+    constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, 0, 0);   // S^T, dP^T: A and B K-major over the head dimension
     constexpr uint32_t idG = idesc_bf16_f32(BK, D, 0, 1);    // dV, dK: A from TMEM, B MN-major [q][d]
     constexpr uint32_t idQ = idesc_bf16_f32(128, BQ, 1, 1);  // dQ^T: A = K^T (MN-major), B = dS^T (MN-major)
     // Operand descriptors are built once; each use only adds a constant byte offset.  K-major views
     // serve S^T and dP^T; MN-major views of the same tiles serve dV, dK and dQ^T.
+    const uint64_t kK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t kV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
     const uint64_t kQ = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
     const uint64_t kDO = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
     const uint64_t mQ = sdesc_sw128(smem_u32(smem + C::kOffQ), C::kChunkQ, 1024);
     const uint64_t mDO = sdesc_sw128(smem_u32(smem + C::kOffDO), C::kChunkQ, 1024);
     const uint64_t mK = sdesc_sw128(smem_u32(smem + C::kOffK), C::kChunkK, 1024);
-    const uint64_t mDS = sdesc_sw128(smem_u32(smem + C::kOffDS), C::kDSBytes, 1024);
+    const uint64_t mDS = sdesc_sw128(smem_u32(smem + C::kOffDS), C::kDSChunk, 1024);
 
-    // S^T = K Q_i^T with K from tensor memory and Q_i K-major over the head dimension.
-    auto s_mma = [&](uint64_t b0, uint32_t dst) {
-        const uint32_t d = tmem + dst, a = tmem + C::kColKA;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk)
-            mma_ts(d, a + kk * 8, sdesc_advance(b0, (kk / 4) * C::kChunkQ + (kk % 4) * 32), idS, kk > 0);
-    };
-    // dP^T = V dO_i^T with both tiles K-major over the head dimension.
+    // X^T = A B^T over the head dimension, both tiles K-major (S^T = K Q^T, dP^T = V dO^T).
     auto qk_like = [&](uint64_t a0, uint64_t b0, uint32_t dst) {
         const uint32_t d = tmem + dst;
 #pragma unroll
@@ -168,116 +214,104 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
             mma_ss(d, sdesc_advance(a0, (kk / 4) * C::kChunkK + (kk % 4) * 32),
                    sdesc_advance(b0, (kk / 4) * C::kChunkQ + (kk % 4) * 32), idS, kk > 0);
     };
-    // G += A[tmem] B_tile with B MN-major over the query block (dV or dK).
-    auto grad = [&](uint32_t a_col, uint64_t b0, uint32_t dst, bool acc) {
-        const uint32_t d = tmem + dst, a = tmem + a_col;
+    // G += A[tmem] B_tile over one half's 64 queries, B MN-major over the head dimension (dV or dK).
+    auto grad = [&](uint32_t a_col, uint64_t b0, int half, uint32_t dst, bool acc) {
+        const uint32_t d = tmem + dst, a = tmem + a_col + half * HQ;
 #pragma unroll
-        for (int kk = 0; kk < BQ / 16; ++kk)
-            mma_ts(d, a + kk * 8, sdesc_advance(b0, kk * 16 * 128), idG, (acc || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < HQ / 16; ++kk)
+            mma_ts(d, a + kk * 8, sdesc_advance(b0, (half * (HQ / 16) + kk) * 16 * 128), idG,
+                   (acc || kk > 0) ? 1u : 0u);
     };
-    // dQ^T = K^T dS^T over the 128 keys, into the step's buffer.
-    auto dq = [&](int buf) {
-        const uint32_t d = tmem + C::col_s(buf);
-        const uint64_t b0 = sdesc_advance(mDS, buf * C::kDSBytes);
+    // dQ^T = K^T dS^T over the 128 keys, into the columns of dP^T (free once dK used dS^T).
+    auto dq = [&]() {
+        const uint32_t d = tmem + C::kColDP;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-            mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(b0, kk * 16 * 128), idQ, kk > 0);
+            mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(mDS, kk * 16 * 128), idQ, kk > 0);
     };
 
-    bool ok = mbar_wait_poll(&bars->kv_full, 0, abort_flag) && mbar_wait_poll(&bars->qdo_full[0], 0, abort_flag) &&
-              mbar_wait_poll(&bars->ka_ready, 0, abort_flag);
+    // S^T of step i+1 is issued right behind dQ^T of step i, so the tensor core does not wait for
+    // dQ^T to be moved out of tensor memory; only dP^T of step i+1, which reuses its columns, does.
+    bool ok = mbar_wait_poll(&bars->kv_full, 0, wc) && mbar_wait_poll(&bars->q_full[0], 0, wc);
     if (ok) {
         tc_fence_after();
-        s_mma(kQ, C::col_s(0));
-        mma_commit(&bars->s_full[0]);
-        qk_like(kV, kDO, C::kColDP);
-        mma_commit(&bars->dp_full);
+        qk_like(kK, kQ, C::kColS);
+        mma_commit(&bars->s_full);
     }
     for (int i = 0; ok && i < Tq; ++i) {
-        const int s = i % kStages;
-        const int s1 = (i + 1) % kStages;
-        const int buf = i & 1;
-        if (i + 1 < Tq) {
-            if (!(ok = mbar_wait_poll(&bars->qdo_full[s1], ((i + 1) / kStages) & 1, abort_flag))) break;
-            // Buffer buf^1 last held dQ^T of step i-1: it must have been drained.
-            if (i > 0 && !(ok = mbar_wait_poll(&bars->dq_empty, (i - 1) & 1, abort_flag))) break;
+        const int s = i % kQStages;
+        const int t = i % C::kDOStages;
+        if (!(ok = mbar_wait_poll(&bars->do_full[t], (i / C::kDOStages) & 1, wc))) break;
+        // The columns of dP^T last held dQ^T of step i-1: it must have been moved out.
+        if (i > 0 && !(ok = mbar_wait_poll(&bars->dq_empty, (i - 1) & 1, wc))) break;
+        tc_fence_after();
+        qk_like(kV, sdesc_advance(kDO, t * C::kQBytes), C::kColDP);
+        mma_commit(&bars->dp_full);
+        const uint64_t bdo = sdesc_advance(mDO, t * C::kQBytes), bq = sdesc_advance(mQ, s * C::kQBytes);
+        for (int h = 0; h < 2; ++h) {
+            if (!(ok = mbar_wait_poll(&bars->p_ready[h], i & 1, wc))) break;
             tc_fence_after();
-            s_mma(sdesc_advance(kQ, s1 * C::kQBytes), C::col_s(buf ^ 1));
-            mma_commit(&bars->s_full[buf ^ 1]);
+            grad(C::kColS, bdo, h, C::kColDV, i > 0 || h > 0);
         }
-        if (!(ok = mbar_wait_poll(&bars->p_ready, i & 1, abort_flag))) break;
-        tc_fence_after();
-        grad(C::col_s(buf), sdesc_advance(mDO, s * C::kQBytes), C::kColDV, i > 0);
-        if (!(ok = mbar_wait_poll(&bars->ds_ready, i & 1, abort_flag))) break;
-        tc_fence_after();
-        grad(C::kColDP, sdesc_advance(mQ, s * C::kQBytes), C::kColDK, i > 0);
-        mma_commit(&bars->qdo_empty[s]);
-        dq(buf);
+        if (!ok) break;
+        mma_commit(&bars->do_empty[t]);
+        for (int h = 0; h < 2; ++h) {
+            if (!(ok = mbar_wait_poll(&bars->ds_ready[h], i & 1, wc))) break;
+            tc_fence_after();
+            grad(C::kColDP, bq, h, C::kColDK, i > 0 || h > 0);
+        }
+        if (!ok) break;
+        dq();
         mma_commit(&bars->dq_full);
-        mma_commit(&bars->ds_free[buf]);
         if (i + 1 < Tq) {
-            qk_like(kV, sdesc_advance(kDO, s1 * C::kQBytes), C::kColDP);
-            mma_commit(&bars->dp_full);
+            const int s1 = (i + 1) % kQStages;
+            if (!(ok = mbar_wait_poll(&bars->q_full[s1], ((i + 1) / kQStages) & 1, wc))) break;
+            tc_fence_after();
+            qk_like(kK, sdesc_advance(kQ, s1 * C::kQBytes), C::kColS);
+            mma_commit(&bars->s_full);
         }
     }
     if (ok) mma_commit(&bars->dkdv_full);
     mma_commit(&bars->mma_done);
-    drain_wait(&bars->mma_done, 0);
+    drain_wait(&bars->mma_done, 0, wc);
 }
 
-// Warps 0-3: thread = key row.  Recomputes P^T, forms dS^T, then writes dK and dV.
+// Warps 0-7.  Thread = key row r of the CTA (tensor-memory lane) in the softmax-gradient part and
+// head-dimension index c in the dQ part; `half` selects queries [64 half, 64 half + 64) of each step.
 template <int D>
-__device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, __nv_bfloat16* __restrict__ dk,
-                             __nv_bfloat16* __restrict__ dv, int head, int k0, int N, int Tq, float scale,
-                             float scale_log2) {
+__device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, float* __restrict__ dq_acc,
+                             __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int head, int k0, int N,
+                             int Tq, int rot, float scale, float scale_log2) {
     using C = BwdCfg<D>;
-    volatile int* abort_flag = &bars->abort;
+    WaitCtl* wc = &bars->wait;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int r = warp * 32 + lane;                       // key row in the block, = TMEM lane
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const int half = warp / 4, quarter = warp % 4;
+    const int r = quarter * 32 + lane;                    // key row in the block, = TMEM lane
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool valid_key = k0 + r < N;
-    uint8_t* ds_tile = smem + C::kOffDS;
+    const bool leader = (threadIdx.x % 128) == 0;
+    const bool dq_lane = r < D;                           // dQ^T rows >= D are the d = 64 padding
+    uint8_t* ds_tile = smem + C::kOffDS + half * C::kDSChunk;
     const float* rows_base = reinterpret_cast<const float*>(smem + C::kOffRows);
-
-    // K row r into tensor memory as packed bf16 pairs: the resident A operand of S^T.
-    if (!warp_wait(&bars->kv_full, 0, abort_flag)) return;
-#pragma unroll
-    for (int c = 0; c < C::kChunks; ++c) {
-        uint32_t w[32];
-        const uint8_t* krow = smem + C::kOffK + c * C::kChunkK + r * 128;
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const uint4 x = *reinterpret_cast<const uint4*>(krow + ((p ^ (r & 7)) << 4));
-            w[4 * p] = x.x;
-            w[4 * p + 1] = x.y;
-            w[4 * p + 2] = x.z;
-            w[4 * p + 3] = x.w;
-        }
-        tmem_st32(tmem + lane_off + C::kColKA + c * 32, w);
-    }
-    tmem_st_wait();
-    tc_fence_before();
-    mbar_arrive(&bars->ka_ready);
+    const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
 
     bool ok = true;
     for (int i = 0; i < Tq; ++i) {
-        const int s = i % kStages;
-        const int buf = i & 1;
-        if (!(ok = warp_wait(&bars->s_full[buf], (i >> 1) & 1, abort_flag))) break;
-        if (!(ok = warp_wait(&bars->qdo_full[s], (i / kStages) & 1, abort_flag))) break;
+        const int s = i % kQStages;
+        if (!(ok = warp_wait(&bars->s_full, i & 1, wc))) break;
+        if (!(ok = warp_wait(&bars->q_full[s], (i / kQStages) & 1, wc))) break;
         tc_fence_after();
-        const float* lse2 = rows_base + s * 2 * BQ;
+        const float* lse2 = rows_base + s * 2 * BQ + half * HQ;
         const float* drow = lse2 + BQ;
-        uint32_t sr[2][32];
-        tmem_ld32(tmem + lane_off + C::col_s(buf), sr[0]);
-        tmem_ld32(tmem + lane_off + C::col_s(buf) + 32, sr[1]);
-        tmem_ld_wait();
-        uint64_t p2[BQ / 2];
+        uint64_t p2[HQ / 2];
         {
-            const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
+            uint32_t sr[2][32];
+            tmem_ld32(tmem + lane_off + C::kColS + half * HQ, sr[0]);
+            tmem_ld32(tmem + lane_off + C::kColS + half * HQ + 32, sr[1]);
+            tmem_ld_wait();
             uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < BQ / 2; ++c) {
+            for (int c = 0; c < HQ / 2; ++c) {
                 const int q = (2 * c) / 32, e = (2 * c) % 32;
                 const uint64_t x2 = ffma2(f2_pack(__uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1])), sl2,
                                           *reinterpret_cast<const uint64_t*>(lse2 + 2 * c));
@@ -287,32 +321,35 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, __
                 p2[c] = f2_pack(p0, p1);
                 pk[c] = pack_bf16(p0, p1);
             }
-            tmem_st32(tmem + lane_off + C::col_s(buf), pk);
+            // P^T as bf16 pairs over the first 32 of this half's 64 columns of S^T.
+            tmem_st32(tmem + lane_off + C::kColS + half * HQ, pk);
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->p_ready);
+        mbar_arrive(&bars->p_ready[half]);
 
-        if (!(ok = warp_wait(&bars->dp_full, i & 1, abort_flag))) break;
+        if (!(ok = warp_wait(&bars->dp_full, i & 1, wc))) break;
         tc_fence_after();
-        uint32_t dr[2][32];
-        tmem_ld32(tmem + lane_off + C::kColDP, dr[0]);
-        tmem_ld32(tmem + lane_off + C::kColDP + 32, dr[1]);
-        tmem_ld_wait();
         uint32_t pk[32];
+        {
+            uint32_t dr[2][32];
+            tmem_ld32(tmem + lane_off + C::kColDP + half * HQ, dr[0]);
+            tmem_ld32(tmem + lane_off + C::kColDP + half * HQ + 32, dr[1]);
+            tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-            const int q = (2 * c) / 32, e = (2 * c) % 32;
-            const uint64_t g2 = fadd2(f2_pack(__uint_as_float(dr[q][e]), __uint_as_float(dr[q][e + 1])),
-                                      *reinterpret_cast<const uint64_t*>(drow + 2 * c));
-            float d0, d1;
-            f2_unpack(fmul2(p2[c], g2), d0, d1);
-            pk[c] = pack_bf16(d0, d1);
+            for (int c = 0; c < HQ / 2; ++c) {
+                const int q = (2 * c) / 32, e = (2 * c) % 32;
+                const uint64_t g2 = fadd2(f2_pack(__uint_as_float(dr[q][e]), __uint_as_float(dr[q][e + 1])),
+                                          *reinterpret_cast<const uint64_t*>(drow + 2 * c));
+                float d0, d1;
+                f2_unpack(fmul2(p2[c], g2), d0, d1);
+                pk[c] = pack_bf16(d0, d1);
+            }
         }
-        tmem_st32(tmem + lane_off + C::kColDP, pk);
-        // dS^T row r into the shared tile (128-byte rows, 16-byte chunks XOR-swizzled by r % 8).
-        if (i >= 2 && !(ok = warp_wait(&bars->ds_free[buf], ((i >> 1) - 1) & 1, abort_flag))) break;
-        uint8_t* row = ds_tile + buf * C::kDSBytes + r * 128;
+        tmem_st32(tmem + lane_off + C::kColDP + half * HQ, pk);
+        // dS^T row r into this half's shared tile (128-byte rows, 16-byte chunks XOR-swizzled by r % 8).
+        // dQ^T of the previous step, the tile's last reader, has completed (this thread saw dq_full).
+        uint8_t* row = ds_tile + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
             *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
@@ -320,82 +357,72 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, __
         fence_proxy_async_smem();
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->ds_ready);
-    }
-    if (!ok) return;
-    if (!warp_wait(&bars->dkdv_full, 0, abort_flag)) return;
-    tc_fence_after();
-    const size_t base = ((size_t)head * N + k0 + r) * D;
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        const uint32_t col = g == 0 ? C::kColDV : C::kColDK;
-        const float mul = g == 0 ? 1.f : scale;
-        __nv_bfloat16* out = g == 0 ? dv : dk;
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-            uint32_t x[32];
-            tmem_ld32(tmem + lane_off + col + q * 32, x);
-            tmem_ld_wait();
-            uint32_t pk2[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                pk2[c] = pack_bf16(__uint_as_float(x[2 * c]) * mul, __uint_as_float(x[2 * c + 1]) * mul);
-            if (valid_key) {
-                uint4* dst = reinterpret_cast<uint4*>(out + base + q * 32);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    dst[c] = make_uint4(pk2[4 * c], pk2[4 * c + 1], pk2[4 * c + 2], pk2[4 * c + 3]);
-            }
-        }
-    }
-}
+        mbar_arrive(&bars->ds_ready[half]);
 
-// Warps 4-7: thread = head-dimension index c.  Moves dQ_i^T out of tensor memory and adds it into the
-// fp32 accumulator [head][N][D] with one bulk reduce-add per query block.
-template <int D>
-__device__ void bwd_dq_drain(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, float* __restrict__ dq_acc, int head,
-                             int N, int Tq) {
-    using C = BwdCfg<D>;
-    volatile int* abort_flag = &bars->abort;
-    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-    const int quarter = warp & 3;
-    const int c = quarter * 32 + lane;
-    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const bool active = quarter * 32 < D;
-    float* stage = reinterpret_cast<float*>(smem + C::kOffDQ);
-    const bool leader = threadIdx.x == 128;
-
-    // Every warp reaches both named barriers in every step, even after a wait gave up, so that no
-    // warp of this group can be left waiting on the others.
-    bool failed = false;
-    for (int i = 0; i < Tq; ++i) {
-        if (!failed && !warp_wait(&bars->dq_full, i & 1, abort_flag)) failed = true;
+        // dQ_i^T: this half's 64 query columns, thread = head-dimension index r.
+        if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
+        tc_fence_after();
         uint32_t x[2][32];
-        if (!failed) {
-            tc_fence_after();
-            if (active) {
-                tmem_ld32(tmem + lane_off + C::col_s(i & 1), x[0]);
-                tmem_ld32(tmem + lane_off + C::col_s(i & 1) + 32, x[1]);
-                tmem_ld_wait();
-            }
-            tc_fence_before();
-            mbar_arrive(&bars->dq_empty);
+        if (dq_lane) {
+            tmem_ld32(tmem + lane_off + C::kColDP + half * HQ, x[0]);
+            tmem_ld32(tmem + lane_off + C::kColDP + half * HQ + 32, x[1]);
+            tmem_ld_wait();
         }
-        if (leader) bulk_wait_group_read<0>();
-        named_bar_sync(1, 128);
-        if (!failed && active) {
+        tc_fence_before();
+        mbar_arrive(&bars->dq_empty);
+        // Stage rows [HQ][D] (fp32): the step's Q tile (first half) or the second half's own buffer.
+        float* stage = reinterpret_cast<float*>(half == 0 ? smem + C::kOffQ + s * C::kQBytes : smem + C::kOffStageB);
+        // The second half's buffer is reused once the reduce of the previous step's rows has read it (it has
+        // had a whole step); only the thread that issued that reduce can wait for it.
+        if (half == 1 && i > 0) {
+            if (leader) {
+                bulk_wait_group_read<0>();
+                mbar_arrive(&bars->stage_b_free);
+            }
+            if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
+        }
+        if (dq_lane) {
 #pragma unroll
-            for (int q = 0; q < BQ; ++q) stage[q * D + c] = __uint_as_float(x[q / 32][q % 32]);
+            for (int q = 0; q < HQ; ++q) stage[q * D + r] = __uint_as_float(x[q / 32][q % 32]);
         }
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (leader && !failed && !*abort_flag) {
-            const int rows = min(BQ, N - i * BQ);
-            bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)i * BQ) * D, stage, (uint32_t)(rows * D * 4));
-            bulk_commit_group();
+        mbar_arrive(half == 0 ? &bars->staged_q[s] : &bars->staged_b);
+        // The TMA thread reduces the first half; the second half's leader reduces its own.  A wait that
+        // gives up has set the abort flag, which stops the whole warp at its next wait.
+        if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
+            const int q0 = qblock(i, rot, Tq) * BQ + HQ;
+            const int rows = min(HQ, N - q0);
+            if (rows > 0) {
+                bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, stage, (uint32_t)(rows * D * 4));
+                bulk_commit_group();
+            }
         }
     }
     if (leader) bulk_wait_group<0>();
+    if (!ok) return;
+    if (!warp_wait(&bars->dkdv_full, 0, wc)) return;
+    tc_fence_after();
+    // Warps 0-3 write dV, warps 4-7 dK (scaled), each thread its key row.
+    const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
+    const float mul = half == 0 ? 1.f : scale;
+    __nv_bfloat16* out = half == 0 ? dv : dk;
+    const size_t base = ((size_t)head * N + k0 + r) * D;
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t y[32];
+        tmem_ld32(tmem + lane_off + col + q * 32, y);
+        tmem_ld_wait();
+        uint32_t pk2[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c)
+            pk2[c] = pack_bf16(__uint_as_float(y[2 * c]) * mul, __uint_as_float(y[2 * c + 1]) * mul);
+        if (valid_key) {
+            uint4* dst = reinterpret_cast<uint4*>(out + base + q * 32);
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                dst[c] = make_uint4(pk2[4 * c], pk2[4 * c + 1], pk2[4 * c + 2], pk2[4 * c + 3]);
+        }
+    }
 }
 
 template <int D>
@@ -407,34 +434,44 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               int blocks_per_head, float scale, float scale_log2, long long wait_budget) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    const uint32_t pad = (1024 - (smem_u32(smem_raw) & 1023)) & 1023;
+    if (pad > C::kAlignSlack) {   // cannot happen without static shared memory; never touch memory past the end
+        if (threadIdx.x == 0) atomicCAS(&g_bwd_status, 0, (int)FA_ERR_CUDA);
+        return;
+    }
+    uint8_t* smem = smem_raw + pad;
     BwdBarriers* bars = reinterpret_cast<BwdBarriers*>(smem + C::kOffBar);
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     // 1-D grid, head-major: the CTAs of one head walk the same Q/dO blocks, which stay in L2.
     const int head = blockIdx.x / blocks_per_head;
     const int k0 = (blockIdx.x % blocks_per_head) * BK;
     const int Tq = Npad / BQ;
+    // Every CTA of a head walks the query blocks starting at its own key-block index, so that at any time
+    // the CTAs add into different dQ rows instead of all contending for the same ones in L2.
+    const int rot = blockIdx.x % blocks_per_head;
 
     if (threadIdx.x == 0) {
-        s_wait_budget = wait_budget;
+        bars->wait.budget = wait_budget;
         mbar_init(&bars->kv_full, 1);
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&bars->qdo_full[s], 1);
-            mbar_init(&bars->qdo_empty[s], 1);
+        for (int s = 0; s < kQStages; ++s) {
+            mbar_init(&bars->q_full[s], 1);
+            mbar_init(&bars->staged_q[s], 128);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&bars->s_full[b], 1);
-            mbar_init(&bars->ds_free[b], 1);
+        for (int t = 0; t < 2; ++t) {
+            mbar_init(&bars->do_full[t], 1);
+            mbar_init(&bars->do_empty[t], 1);
+            mbar_init(&bars->p_ready[t], 128);
+            mbar_init(&bars->ds_ready[t], 128);
         }
+        mbar_init(&bars->staged_b, 128);
+        mbar_init(&bars->s_full, 1);
         mbar_init(&bars->dp_full, 1);
-        mbar_init(&bars->p_ready, 128);
-        mbar_init(&bars->ds_ready, 128);
         mbar_init(&bars->dq_full, 1);
-        mbar_init(&bars->dq_empty, 128);
+        mbar_init(&bars->dq_empty, 256);
+        mbar_init(&bars->stage_b_free, 1);
         mbar_init(&bars->dkdv_full, 1);
-        mbar_init(&bars->ka_ready, 128);
         mbar_init(&bars->mma_done, 1);
-        bars->abort = 0;
+        bars->wait.abort = 0;
         fence_mbar_init();
     }
     if constexpr (C::kZeroBytes > 0) {
@@ -458,13 +495,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t tmem = bars->tmem_base;
 
     if (warp == kTmaWarp) {
-        if (lane == 0) bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, lse2, row_d, smem, bars, head, k0, Tq, Npad);
+        if (lane == 0)
+            bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, lse2, row_d, dq_acc, smem, bars, head, k0, N, Tq, Npad, rot);
     } else if (warp == kMmaWarp) {
         if (lane == 0) bwd_mma<D>(smem, bars, tmem, Tq);
-    } else if (warp < 4) {
-        bwd_softgrad<D>(smem, bars, tmem, dk, dv, head, k0, N, Tq, scale, scale_log2);
     } else {
-        bwd_dq_drain<D>(smem, bars, tmem, dq_acc, head, N, Tq);
+        bwd_softgrad<D>(smem, bars, tmem, dq_acc, dk, dv, head, k0, N, Tq, rot, scale, scale_log2);
     }
 
     tc_fence_before();
@@ -473,7 +509,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
-    if (threadIdx.x == 0 && bars->abort) atomicCAS(&g_bwd_status, 0, (int)FA_ERR_TIMEOUT);
+    if (threadIdx.x == 0 && bars->wait.abort) atomicCAS(&g_bwd_status, 0, (int)FA_ERR_TIMEOUT);
 }
 
 // -D_i = -(dO_i . O_i) and -LSE2_i = -LSE_i log2(e) into [head][Npad] arrays (pad rows: 0 and -inf);

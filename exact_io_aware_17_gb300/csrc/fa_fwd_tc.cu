@@ -65,7 +65,7 @@ struct FwdBarriers {
     uint64_t o_full[2];
     uint64_t mma_done;
     uint32_t tmem_base;
-    int abort;
+    WaitCtl wait;
 };
 
 template <int D>
@@ -90,7 +90,7 @@ template <int D>
 __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v, uint8_t* smem,
                          FwdBarriers* bars, int head, int q0, int kv0, int T, int starve) {
     using C = FwdCfg<D>;
-    volatile int* abort_flag = &bars->abort;
+    WaitCtl* wc = &bars->wait;
     const uint64_t pol_kv = policy_evict_last();
     const uint64_t pol_q = policy_evict_first();
     // starve != 0 withholds the Q loads so that the MMA warp's first wait runs out: the failure path
@@ -104,7 +104,7 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
     int issued = 0;
     for (int j = 0; j < T; ++j) {
         const int s = j % C::kStages;
-        if (j >= C::kStages && !mbar_wait(&bars->kv_empty[s], ((j / C::kStages) - 1) & 1, abort_flag)) break;
+        if (j >= C::kStages && !mbar_wait(&bars->kv_empty[s], ((j / C::kStages) - 1) & 1, wc)) break;
         mbar_expect_tx(&bars->k_full[s], C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffK + s * C::kKVBytes + c * C::kChunkKV, tm_k, &bars->k_full[s], c * 64,
@@ -116,18 +116,18 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
         issued = j + 1;
     }
     // Every load issued must have landed before the CTA may exit (only matters after an abort).
-    drain_wait(&bars->q_full[0], 0);
-    drain_wait(&bars->q_full[1], 0);
+    drain_wait(&bars->q_full[0], 0, wc);
+    drain_wait(&bars->q_full[1], 0, wc);
     for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j) {
-        drain_wait(&bars->k_full[j % C::kStages], (j / C::kStages) & 1);
-        drain_wait(&bars->v_full[j % C::kStages], (j / C::kStages) & 1);
+        drain_wait(&bars->k_full[j % C::kStages], (j / C::kStages) & 1, wc);
+        drain_wait(&bars->v_full[j % C::kStages], (j / C::kStages) & 1, wc);
     }
 }
 
 template <int D>
 __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int T) {
     using C = FwdCfg<D>;
-    volatile int* abort_flag = &bars->abort;
+    WaitCtl* wc = &bars->wait;
     constexpr uint32_t idS = idesc_bf16_f32(BM, BN, 0, 0);
     constexpr uint32_t idPV = idesc_bf16_f32(BM, D, 0, 1);
     // Operand descriptors are built once; each k-step only adds a constant byte offset.
@@ -154,12 +154,12 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
             mma_ts(d, a + kk * 8, sdesc_advance(b0, kk * 16 * 128), idPV, (accumulate || kk > 0) ? 1u : 0u);
     };
 
-    bool ok = mbar_wait_poll(&bars->q_full[0], 0, abort_flag) && mbar_wait_poll(&bars->q_full[1], 0, abort_flag);
+    bool ok = mbar_wait_poll(&bars->q_full[0], 0, wc) && mbar_wait_poll(&bars->q_full[1], 0, wc);
     for (int j = 0; ok && j < T; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
         if (j == 0) {
-            if (!(ok = mbar_wait_poll(&bars->k_full[s], ph, abort_flag))) break;
+            if (!(ok = mbar_wait_poll(&bars->k_full[s], ph, wc))) break;
             tc_fence_after();
             issue_s(0, s);
             mma_commit(&bars->s_full[0]);
@@ -168,18 +168,18 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
         }
         const int s2 = (j + 1) % C::kStages;
         const uint32_t ph2 = ((j + 1) / C::kStages) & 1;
-        if (!(ok = mbar_wait_poll(&bars->v_full[s], ph, abort_flag))) break;
-        if (!(ok = mbar_wait_poll(&bars->p_full[0], j & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_poll(&bars->v_full[s], ph, wc))) break;
+        if (!(ok = mbar_wait_poll(&bars->p_full[0], j & 1, wc))) break;
         tc_fence_after();
         issue_pv(0, s, j > 0);
         if (j == T - 1) mma_commit(&bars->o_full[0]);
         if (j + 1 < T) {
-            if (!(ok = mbar_wait_poll(&bars->k_full[s2], ph2, abort_flag))) break;
+            if (!(ok = mbar_wait_poll(&bars->k_full[s2], ph2, wc))) break;
             tc_fence_after();
             issue_s(0, s2);
             mma_commit(&bars->s_full[0]);
         }
-        if (!(ok = mbar_wait_poll(&bars->p_full[1], j & 1, abort_flag))) break;
+        if (!(ok = mbar_wait_poll(&bars->p_full[1], j & 1, wc))) break;
         tc_fence_after();
         issue_pv(1, s, j > 0);
         mma_commit(&bars->kv_empty[s]);
@@ -191,7 +191,7 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
     }
     // Tensor memory is freed after this: every MMA issued must have completed.
     mma_commit(&bars->mma_done);
-    drain_wait(&bars->mma_done, 0);
+    drain_wait(&bars->mma_done, 0, wc);
 }
 
 template <int D, bool kStepNorm>
@@ -199,7 +199,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
                            float* __restrict__ lse, int head, int q0, int N, int kv0, int T, int T_all,
                            float scale_log2, float* ml_out) {
     using C = FwdCfg<D>;
-    volatile int* abort_flag = &bars->abort;
+    WaitCtl* wc = &bars->wait;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quarter = warp & 3;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -210,7 +210,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-        if (!(ok = warp_wait(&bars->s_full[t], j & 1, abort_flag))) break;
+        if (!(ok = warp_wait(&bars->s_full[t], j & 1, wc))) break;
         tc_fence_after();
         uint32_t r[4][32];
 #pragma unroll
@@ -331,7 +331,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
         mbar_arrive(&bars->p_full[t]);
     }
     if (!ok) return;
-    if (!warp_wait(&bars->o_full[t], 0, abort_flag)) return;
+    if (!warp_wait(&bars->o_full[t], 0, wc)) return;
     tc_fence_after();
     if (ml_out) {  // one half of a split pair: O stays in TMEM, m and l go to shared memory for the merge
         ml_out[t * BM + quarter * 32 + lane] = m_run;
@@ -448,7 +448,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const int T = split ? (rank ? T_all - T_all / 2 : T_all / 2) : T_all;
 
     if (threadIdx.x == 0) {
-        s_wait_budget = wait_budget;
+        bars->wait.budget = wait_budget;
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->q_full[t], 1);
             mbar_init(&bars->s_full[t], 1);
@@ -461,7 +461,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&bars->kv_empty[s], 1);
         }
         mbar_init(&bars->mma_done, 1);
-        bars->abort = 0;
+        bars->wait.abort = 0;
         fence_mbar_init();
     }
     if (warp == kTmaWarp && lane == 0) {
@@ -493,7 +493,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         // Every thread of both CTAs reaches both cluster barriers: all waits before them are bounded.
         cluster_sync();  // both halves done: rank 0's K/V and Q buffers are free to receive
         tc_fence_after();
-        const bool both_ok = !bars->abort;
+        const bool both_ok = !bars->wait.abort;
         if (rank == 1 && warp < 8 && both_ok) split_send<D>(smem, tmem, warp / 4);
         cluster_sync();  // rank 1's stores are visible to rank 0
         if (rank == 0 && warp < 8 && both_ok) split_merge<D>(smem, tmem, warp / 4, o, lse, head, q0, N);
@@ -504,7 +504,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemCols);
     }
-    if (threadIdx.x == 0 && bars->abort) atomicCAS(&g_fwd_status, 0, (int)FA_ERR_TIMEOUT);
+    if (threadIdx.x == 0 && bars->wait.abort) atomicCAS(&g_fwd_status, 0, (int)FA_ERR_TIMEOUT);
 }
 
 template <int D, bool kStepNorm>

@@ -30,8 +30,8 @@ struct BwdWorkspace {
     size_t dq_acc, row_d, lse2, total;
 };
 BwdWorkspace bwd_workspace_layout(const Shape& s);
-// Rows per head of the backward's per-row arrays: N rounded up to the 64-query block of the kernel.
-inline int bwd_padded_rows(int N) { return (N + 63) / 64 * 64; }
+// Rows per head of the backward's per-row arrays: N rounded up to the 128-query step of the kernel.
+inline int bwd_padded_rows(int N) { return (N + 127) / 128 * 128; }
 
 // Budget of the kernels' bounded waits, and the test switch that makes the forward's first wait run
 // out (FA_TEST_STARVE_WAIT=1 in the environment: the Q loads are withheld and the budget is ~10 ms).

@@ -51,20 +51,29 @@ __device__ __forceinline__ bool mbar_poll(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Clock budget of one wait, in cycles.  A wait that runs out of it reports a timeout instead of spinning
-// forever.  Each kernel copies the budget its launcher passes (about two seconds of clock normally;
-// ~10 ms in the tests that make a wait run out on purpose) into s_wait_budget before any wait.
-static __shared__ long long s_wait_budget;
+// Wait state of one CTA, kept in its dynamic shared memory (so that kernels need no static shared
+// memory and their dynamic region starts 1024-byte aligned).  `budget` is the clock budget of one wait, in
+// cycles: a wait that runs out of it reports a timeout instead of spinning forever.  Each kernel stores
+// the budget its launcher passes (about two seconds of clock normally; ~10 ms in the tests that make a
+// wait run out on purpose) before any wait.  `abort` becomes nonzero once any wait of the CTA has given
+// up; every other wait then returns at once and the CTA winds down.
+struct WaitCtl {
+    int abort;
+    int reserved;
+    long long budget;
+};
 
-// Waits for the phase with the given parity to complete.  Returns false if the budget ran out or
-// `abort_flag` (shared) became nonzero; the caller then winds down.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+// Waits for the phase with the given parity to complete.  Returns false if the budget ran out or the
+// CTA's abort flag became nonzero; the caller then winds down.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, WaitCtl* wc) {
     if (mbar_test(bar, parity)) return true;
+    volatile int* abort_flag = &wc->abort;
+    const long long budget = wc->budget;
     const long long t0 = clock64();
     while (true) {
         if (mbar_test(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > s_wait_budget) {
+        if (clock64() - t0 > budget) {
             *abort_flag = 1;
             return false;
         }
@@ -74,13 +83,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 // As mbar_wait, but polls without suspending.  For the single MMA-issuing thread: a suspended
 // try_wait was measured to notice a completed phase some 400 cycles late, and the tensor core idles
 // for that long; one polling thread costs the other warps little issue bandwidth.
-__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+__device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, WaitCtl* wc) {
     if (mbar_poll(bar, parity)) return true;
+    volatile int* abort_flag = &wc->abort;
+    const long long budget = wc->budget;
     const long long t0 = clock64();
     while (true) {
         if (mbar_poll(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (clock64() - t0 > s_wait_budget) {
+        if (clock64() - t0 > budget) {
             *abort_flag = 1;
             return false;
         }
@@ -88,15 +99,16 @@ __device__ __forceinline__ bool mbar_wait_poll(uint64_t* bar, uint32_t parity, v
 }
 
 // Waits that run out of budget, or see another warp's abort, make the whole warp stop.
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
-    bool ok = mbar_wait(bar, parity, abort_flag);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, WaitCtl* wc) {
+    bool ok = mbar_wait(bar, parity, wc);
     return __all_sync(0xffffffffu, ok);
 }
 
 // Waits with a fixed budget and no abort check: used to drain copies in flight before exit.
-__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const WaitCtl* wc) {
+    const long long budget = wc->budget;
     const long long t0 = clock64();
-    while (!mbar_test(bar, parity) && clock64() - t0 < s_wait_budget) {
+    while (!mbar_test(bar, parity) && clock64() - t0 < budget) {
     }
 }
 

@@ -81,7 +81,7 @@ fa_status fa_fwd_f32(const float* q, const float* k, const float* v, float* o, f
 
 /*
  * fa_bwd_workspace_size — bytes of device scratch fa_bwd needs for this shape: an fp32 dQ accumulator
- * [B,H,N,d] and two fp32 per-row arrays [B,H,Np] with Np = N rounded up to a multiple of 64 (the
+ * [B,H,N,d] and two fp32 per-row arrays [B,H,Np] with Np = N rounded up to a multiple of 128 (the
  * negated row term -D_i = -dO_i . O_i and the negated log2-domain LSE), each section rounded up to 256
  * bytes.  Returns 0 for invalid shapes.
  */

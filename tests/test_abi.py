@@ -106,7 +106,7 @@ def test_workspace_size_formula(fa):
         return (x + 255) // 256 * 256
     for B, H, N, d in ((1, 1, 1, 64), (4, 16, 2048, 64), (1, 16, 8192, 128), (2, 3, 100, 128)):
         rows = B * H * N
-        padded = B * H * ((N + 63) // 64 * 64)
+        padded = B * H * ((N + 127) // 128 * 128)
         assert fa.fa_bwd_workspace_size(B, H, N, d) == r256(rows * d * 4) + 2 * r256(padded * 4)
     assert fa.fa_bwd_workspace_size(0, 1, 1, 64) == 0
 
