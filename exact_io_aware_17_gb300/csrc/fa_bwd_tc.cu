@@ -62,14 +62,14 @@ constexpr int HQ = 64;   // queries per warpgroup half of a step
 constexpr int kThreads = 320;
 constexpr int kTmaWarp = 8;
 constexpr int kMmaWarp = 9;
-constexpr int kQStages = 2;
 
 struct BwdBarriers {
     uint64_t kv_full;
-    uint64_t q_full[kQStages];     // Q tile + LSE2 and -D rows of a step
-    uint64_t staged_q[kQStages];   // the first half's dQ rows are staged in this Q tile
-    uint64_t do_full[2];
-    uint64_t do_empty[2];
+    uint64_t q_full[2];            // Q tile + LSE2 and -D rows of a step
+    uint64_t q_empty[2];           // dK of that step has read the Q tile
+    uint64_t do_full[2];           // dO tile of a step in its slot
+    uint64_t dv_done[2];           // dV of that step has read dO: the slot takes dS^T
+    uint64_t staged_a[2];          // the first half's dQ rows are in the slot
     uint64_t s_full;
     uint64_t dp_full;
     uint64_t p_ready[2];
@@ -84,27 +84,31 @@ struct BwdBarriers {
     WaitCtl wait;
 };
 
+// Shared memory.  K and V stay resident; Q has two stages.  Each step's dO tile lives in one of two
+// slots, and the slot is reused within the step: once dV has read dO it takes the step's dS^T (the B
+// operand of dQ^T), and once dQ^T has read that it takes the first half's fp32 dQ rows, which the TMA
+// thread adds into the accumulator before loading the dO tile of step i + 2 there.  The second half's
+// dQ rows have a buffer of their own.
 template <int D>
 struct BwdCfg {
     static constexpr int kChunks = D / 64;
-    static constexpr int kDOStages = D == 64 ? 2 : 1;
     static constexpr uint32_t kChunkK = BK * 128;          // one 64-column chunk of a K or V tile
     static constexpr uint32_t kChunkQ = BQ * 128;          // one 64-column chunk of a Q or dO tile
     static constexpr uint32_t kKBytes = BK * D * 2;
     static constexpr uint32_t kQBytes = BQ * D * 2;
+    static constexpr uint32_t kDSChunk = BK * 128;         // dS^T of one half: 128 key rows x 64 queries
+    static constexpr uint32_t kHalfDQBytes = HQ * D * 4;   // fp32 dQ rows [HQ][D] of one half
+    static constexpr uint32_t kSlotBytes = 2 * kDSChunk;   // holds a dO tile, dS^T or a half's dQ rows
     static constexpr uint32_t kOffK = 0;
     static constexpr uint32_t kOffZero = kOffK + kKBytes;   // d = 64: zero half that pads K^T to M = 128
     static constexpr uint32_t kZeroBytes = (D == 64) ? kChunkK : 0;
     static constexpr uint32_t kOffV = kOffZero + kZeroBytes;
     static constexpr uint32_t kOffQ = kOffV + kKBytes;
-    static constexpr uint32_t kOffDO = kOffQ + kQStages * kQBytes;
-    static constexpr uint32_t kDSChunk = BK * 128;         // dS^T of one half: 128 key rows x 64 queries
-    static constexpr uint32_t kOffDS = kOffDO + kDOStages * kQBytes;
-    static constexpr uint32_t kHalfDQBytes = HQ * D * 4;   // fp32 dQ rows [HQ][D] of one half
-    static constexpr uint32_t kOffStageB = kOffDS + 2 * kDSChunk;   // the second half's dQ rows
+    static constexpr uint32_t kOffSlot = kOffQ + 2 * kQBytes;
+    static constexpr uint32_t kOffStageB = kOffSlot + 2 * kSlotBytes;   // the second half's dQ rows
     static constexpr uint32_t kRowBytes = BQ * 4;          // LSE2 or -D of one query block
-    static constexpr uint32_t kOffRows = kOffStageB + kHalfDQBytes;  // [q stage][LSE2 | -D][BQ] floats
-    static constexpr uint32_t kOffBar = kOffRows + kQStages * 2 * kRowBytes;
+    static constexpr uint32_t kOffRows = kOffStageB + kHalfDQBytes;    // [q stage][LSE2 | -D][BQ] floats
+    static constexpr uint32_t kOffBar = kOffRows + 2 * 2 * kRowBytes;
     static constexpr uint32_t kSmemNeed = kOffBar + sizeof(BwdBarriers);
     // Room to align the region to 1024 bytes if the dynamic shared memory does not start aligned (it
     // does when the kernel has no static shared memory, which is the case here).
@@ -112,7 +116,7 @@ struct BwdCfg {
     static constexpr uint32_t kSmemBytes = kSmemNeed + kAlignSlack;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
     static constexpr uint32_t kTmemCols = 512;
-    static_assert(kHalfDQBytes == kQBytes, "the first half's dQ rows are staged in the step's Q tile");
+    static_assert(kQBytes <= kSlotBytes && kHalfDQBytes <= kSlotBytes, "slot contents");
     static_assert(kSmemNeed <= 232448, "shared memory per CTA");
 };
 
@@ -135,15 +139,15 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         tma_load_3d(smem + C::kOffK + c * C::kChunkK, tm_k, &bars->kv_full, c * 64, k0, head, pol_keep);
         tma_load_3d(smem + C::kOffV + c * C::kChunkK, tm_v, &bars->kv_full, c * 64, k0, head, pol_keep);
     }
-    // The first half's dQ rows of step j are staged in Q tile j % kQStages.  This thread adds them into
-    // the accumulator and reloads the tile once the reduce has read it, so it owns the tile's whole cycle.
+    // The first half's dQ rows of step j end up in slot j % 2.  This thread adds them into the
+    // accumulator and reloads the slot once the reduce has read it, so it owns the slot's whole cycle.
     auto reduce_first_half = [&](int j) -> bool {
-        const int s = j % kQStages;
-        if (!mbar_wait(&bars->staged_q[s], (j / kQStages) & 1, wc)) return false;
+        const int t = j & 1;
+        if (!mbar_wait(&bars->staged_a[t], (j >> 1) & 1, wc)) return false;
         const int q0 = qblock(j, rot, Tq) * BQ;
         const int rows = min(HQ, N - q0);
         if (rows > 0) {
-            bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, smem + C::kOffQ + s * C::kQBytes,
+            bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, smem + C::kOffSlot + t * C::kSlotBytes,
                                 (uint32_t)(rows * D * 4));
             bulk_commit_group();
         }
@@ -152,12 +156,9 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
     int q_issued = 0, do_issued = 0;
     bool ok = true;
     for (int i = 0; i < Tq && ok; ++i) {
-        const int s = i % kQStages;
-        if (i >= kQStages) {
-            if (!(ok = reduce_first_half(i - kQStages))) break;
-            bulk_wait_group_read<0>();
-        }
+        const int s = i & 1;
         const int qb = qblock(i, rot, Tq);
+        if (i >= 2 && !(ok = mbar_wait(&bars->q_empty[s], ((i >> 1) - 1) & 1, wc))) break;
         uint64_t* bar = &bars->q_full[s];
         mbar_expect_tx(bar, C::kQBytes + 2 * C::kRowBytes);
         for (int c = 0; c < C::kChunks; ++c)
@@ -168,26 +169,28 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         bulk_load(rows + BQ, row_d + r0, C::kRowBytes, bar);
         q_issued = i + 1;
 
-        const int t = i % C::kDOStages;
-        if (i >= C::kDOStages &&
-            !(ok = mbar_wait(&bars->do_empty[t], ((i / C::kDOStages) - 1) & 1, wc)))
-            break;
-        mbar_expect_tx(&bars->do_full[t], C::kQBytes);
+        if (i >= 2) {
+            if (!(ok = reduce_first_half(i - 2))) break;
+            bulk_wait_group_read<0>();
+        }
+        mbar_expect_tx(&bars->do_full[s], C::kQBytes);
         for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem + C::kOffDO + t * C::kQBytes + c * C::kChunkQ, tm_do, &bars->do_full[t], c * 64, qb * BQ,
-                        head, pol_keep);
+            tma_load_3d(smem + C::kOffSlot + s * C::kSlotBytes + c * C::kChunkQ, tm_do, &bars->do_full[s], c * 64,
+                        qb * BQ, head, pol_keep);
         do_issued = i + 1;
     }
-    for (int j = (Tq > kQStages ? Tq - kQStages : 0); ok && j < Tq; ++j) ok = reduce_first_half(j);
+    for (int j = (Tq > 2 ? Tq - 2 : 0); ok && j < Tq; ++j) ok = reduce_first_half(j);
     bulk_wait_group<0>();
     // Copies still in flight must land before the CTA can exit.
     drain_wait(&bars->kv_full, 0, wc);
-    for (int i = (q_issued > kQStages ? q_issued - kQStages : 0); i < q_issued; ++i)
-        drain_wait(&bars->q_full[i % kQStages], (i / kQStages) & 1, wc);
-    for (int i = (do_issued > C::kDOStages ? do_issued - C::kDOStages : 0); i < do_issued; ++i)
-        drain_wait(&bars->do_full[i % C::kDOStages], (i / C::kDOStages) & 1, wc);
+    for (int i = (q_issued > 2 ? q_issued - 2 : 0); i < q_issued; ++i) drain_wait(&bars->q_full[i & 1], (i >> 1) & 1, wc);
+    for (int i = (do_issued > 2 ? do_issued - 2 : 0); i < do_issued; ++i)
+        drain_wait(&bars->do_full[i & 1], (i >> 1) & 1, wc);
 }
 
+// MMA order of step i: dV(i), S^T(i+1), dK(i), dQ^T(i), dP^T(i+1).  S^T of the next step goes right
+// behind dV (its columns held P^T, which dV has just read), so the softmax warps can form P(i+1) while
+// the tensor core works on dK and dQ^T; dP^T(i+1) waits until dQ^T(i) has left its columns.
 template <int D>
 __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq) {
     using C = BwdCfg<D>;
@@ -200,11 +203,11 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
     const uint64_t kK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t kV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
     const uint64_t kQ = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
-    const uint64_t kDO = sdesc_sw128(smem_u32(smem + C::kOffDO), 16, 1024);
+    const uint64_t kDO = sdesc_sw128(smem_u32(smem + C::kOffSlot), 16, 1024);
     const uint64_t mQ = sdesc_sw128(smem_u32(smem + C::kOffQ), C::kChunkQ, 1024);
-    const uint64_t mDO = sdesc_sw128(smem_u32(smem + C::kOffDO), C::kChunkQ, 1024);
+    const uint64_t mDO = sdesc_sw128(smem_u32(smem + C::kOffSlot), C::kChunkQ, 1024);
     const uint64_t mK = sdesc_sw128(smem_u32(smem + C::kOffK), C::kChunkK, 1024);
-    const uint64_t mDS = sdesc_sw128(smem_u32(smem + C::kOffDS), C::kDSChunk, 1024);
+    const uint64_t mDS = sdesc_sw128(smem_u32(smem + C::kOffSlot), C::kDSChunk, 1024);
 
     // X^T = A B^T over the head dimension, both tiles K-major (S^T = K Q^T, dP^T = V dO^T).
     auto qk_like = [&](uint64_t a0, uint64_t b0, uint32_t dst) {
@@ -223,52 +226,56 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
                    (acc || kk > 0) ? 1u : 0u);
     };
     // dQ^T = K^T dS^T over the 128 keys, into the columns of dP^T (free once dK used dS^T).
-    auto dq = [&]() {
+    auto dq = [&](uint64_t b0) {
         const uint32_t d = tmem + C::kColDP;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
-            mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(mDS, kk * 16 * 128), idQ, kk > 0);
+            mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(b0, kk * 16 * 128), idQ, kk > 0);
     };
 
-    // S^T of step i+1 is issued right behind dQ^T of step i, so the tensor core does not wait for
-    // dQ^T to be moved out of tensor memory; only dP^T of step i+1, which reuses its columns, does.
     bool ok = mbar_wait_poll(&bars->kv_full, 0, wc) && mbar_wait_poll(&bars->q_full[0], 0, wc);
     if (ok) {
         tc_fence_after();
         qk_like(kK, kQ, C::kColS);
         mma_commit(&bars->s_full);
+        if ((ok = mbar_wait_poll(&bars->do_full[0], 0, wc))) {
+            tc_fence_after();
+            qk_like(kV, kDO, C::kColDP);
+            mma_commit(&bars->dp_full);
+        }
     }
     for (int i = 0; ok && i < Tq; ++i) {
-        const int s = i % kQStages;
-        const int t = i % C::kDOStages;
-        if (!(ok = mbar_wait_poll(&bars->do_full[t], (i / C::kDOStages) & 1, wc))) break;
-        // The columns of dP^T last held dQ^T of step i-1: it must have been moved out.
-        if (i > 0 && !(ok = mbar_wait_poll(&bars->dq_empty, (i - 1) & 1, wc))) break;
-        tc_fence_after();
-        qk_like(kV, sdesc_advance(kDO, t * C::kQBytes), C::kColDP);
-        mma_commit(&bars->dp_full);
-        const uint64_t bdo = sdesc_advance(mDO, t * C::kQBytes), bq = sdesc_advance(mQ, s * C::kQBytes);
+        const int s = i & 1, s1 = s ^ 1;
+        const uint64_t bdo = sdesc_advance(mDO, s * C::kSlotBytes), bq = sdesc_advance(mQ, s * C::kQBytes);
         for (int h = 0; h < 2; ++h) {
             if (!(ok = mbar_wait_poll(&bars->p_ready[h], i & 1, wc))) break;
             tc_fence_after();
             grad(C::kColS, bdo, h, C::kColDV, i > 0 || h > 0);
         }
         if (!ok) break;
-        mma_commit(&bars->do_empty[t]);
+        mma_commit(&bars->dv_done[s]);
+        if (i + 1 < Tq) {
+            if (!(ok = mbar_wait_poll(&bars->q_full[s1], ((i + 1) >> 1) & 1, wc))) break;
+            tc_fence_after();
+            qk_like(kK, sdesc_advance(kQ, s1 * C::kQBytes), C::kColS);
+            mma_commit(&bars->s_full);
+        }
         for (int h = 0; h < 2; ++h) {
             if (!(ok = mbar_wait_poll(&bars->ds_ready[h], i & 1, wc))) break;
             tc_fence_after();
             grad(C::kColDP, bq, h, C::kColDK, i > 0 || h > 0);
         }
         if (!ok) break;
-        dq();
+        mma_commit(&bars->q_empty[s]);
+        dq(sdesc_advance(mDS, s * C::kSlotBytes));
         mma_commit(&bars->dq_full);
         if (i + 1 < Tq) {
-            const int s1 = (i + 1) % kQStages;
-            if (!(ok = mbar_wait_poll(&bars->q_full[s1], ((i + 1) / kQStages) & 1, wc))) break;
+            if (!(ok = mbar_wait_poll(&bars->do_full[s1], ((i + 1) >> 1) & 1, wc))) break;
+            // The columns of dP^T hold dQ^T of step i until it has been moved out.
+            if (!(ok = mbar_wait_poll(&bars->dq_empty, i & 1, wc))) break;
             tc_fence_after();
-            qk_like(kK, sdesc_advance(kQ, s1 * C::kQBytes), C::kColS);
-            mma_commit(&bars->s_full);
+            qk_like(kV, sdesc_advance(kDO, s1 * C::kSlotBytes), C::kColDP);
+            mma_commit(&bars->dp_full);
         }
     }
     if (ok) mma_commit(&bars->dkdv_full);
@@ -277,7 +284,8 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
 }
 
 // Warps 0-7.  Thread = key row r of the CTA (tensor-memory lane) in the softmax-gradient part and
-// head-dimension index c in the dQ part; `half` selects queries [64 half, 64 half + 64) of each step.
+// head-dimension index r in the dQ part; `half` selects queries [64 half, 64 half + 64) of each step.
+// Order of step i: dS(i), P(i+1), then dQ(i) out of tensor memory (P(0) comes first).
 template <int D>
 __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, float* __restrict__ dq_acc,
                              __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int head, int k0, int N,
@@ -291,45 +299,47 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
     const bool valid_key = k0 + r < N;
     const bool leader = (threadIdx.x % 128) == 0;
     const bool dq_lane = r < D;                           // dQ^T rows >= D are the d = 64 padding
-    uint8_t* ds_tile = smem + C::kOffDS + half * C::kDSChunk;
     const float* rows_base = reinterpret_cast<const float*>(smem + C::kOffRows);
     const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
 
-    bool ok = true;
-    for (int i = 0; i < Tq; ++i) {
-        const int s = i % kQStages;
-        if (!(ok = warp_wait(&bars->s_full, i & 1, wc))) break;
-        if (!(ok = warp_wait(&bars->q_full[s], (i / kQStages) & 1, wc))) break;
+    // P(j) for this half: P^T as bf16 pairs over the first 32 of the half's 64 columns of S^T; the fp32
+    // values stay in p2 for dS(j).
+    uint64_t p2[HQ / 2];
+    auto form_p = [&](int j) -> bool {
+        if (!warp_wait(&bars->s_full, j & 1, wc)) return false;
+        if (!warp_wait(&bars->q_full[j & 1], (j >> 1) & 1, wc)) return false;
         tc_fence_after();
-        const float* lse2 = rows_base + s * 2 * BQ + half * HQ;
-        const float* drow = lse2 + BQ;
-        uint64_t p2[HQ / 2];
-        {
-            uint32_t sr[2][32];
-            tmem_ld32(tmem + lane_off + C::kColS + half * HQ, sr[0]);
-            tmem_ld32(tmem + lane_off + C::kColS + half * HQ + 32, sr[1]);
-            tmem_ld_wait();
-            uint32_t pk[32];
+        const float* lse2 = rows_base + (j & 1) * 2 * BQ + half * HQ;
+        uint32_t sr[2][32];
+        tmem_ld32(tmem + lane_off + C::kColS + half * HQ, sr[0]);
+        tmem_ld32(tmem + lane_off + C::kColS + half * HQ + 32, sr[1]);
+        tmem_ld_wait();
+        uint32_t pk[32];
 #pragma unroll
-            for (int c = 0; c < HQ / 2; ++c) {
-                const int q = (2 * c) / 32, e = (2 * c) % 32;
-                const uint64_t x2 = ffma2(f2_pack(__uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1])), sl2,
-                                          *reinterpret_cast<const uint64_t*>(lse2 + 2 * c));
-                float x0, x1;
-                f2_unpack(x2, x0, x1);
-                const float p0 = valid_key ? ex2(x0) : 0.f, p1 = valid_key ? ex2(x1) : 0.f;
-                p2[c] = f2_pack(p0, p1);
-                pk[c] = pack_bf16(p0, p1);
-            }
-            // P^T as bf16 pairs over the first 32 of this half's 64 columns of S^T.
-            tmem_st32(tmem + lane_off + C::kColS + half * HQ, pk);
+        for (int c = 0; c < HQ / 2; ++c) {
+            const int q = (2 * c) / 32, e = (2 * c) % 32;
+            const uint64_t x2 = ffma2(f2_pack(__uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1])), sl2,
+                                      *reinterpret_cast<const uint64_t*>(lse2 + 2 * c));
+            float x0, x1;
+            f2_unpack(x2, x0, x1);
+            const float p0 = valid_key ? ex2(x0) : 0.f, p1 = valid_key ? ex2(x1) : 0.f;
+            p2[c] = f2_pack(p0, p1);
+            pk[c] = pack_bf16(p0, p1);
         }
+        tmem_st32(tmem + lane_off + C::kColS + half * HQ, pk);
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->p_ready[half]);
+        return true;
+    };
 
+    bool ok = Tq > 0 && form_p(0);
+    for (int i = 0; ok && i < Tq; ++i) {
+        const int s = i & 1;
+        // dS(i) = P(i) o (dP(i) - D).
         if (!(ok = warp_wait(&bars->dp_full, i & 1, wc))) break;
         tc_fence_after();
+        const float* drow = rows_base + s * 2 * BQ + BQ + half * HQ;
         uint32_t pk[32];
         {
             uint32_t dr[2][32];
@@ -347,9 +357,10 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
             }
         }
         tmem_st32(tmem + lane_off + C::kColDP + half * HQ, pk);
-        // dS^T row r into this half's shared tile (128-byte rows, 16-byte chunks XOR-swizzled by r % 8).
-        // dQ^T of the previous step, the tile's last reader, has completed (this thread saw dq_full).
-        uint8_t* row = ds_tile + r * 128;
+        // dS^T row r into this half's chunk of the step's slot (128-byte rows, 16-byte chunks XOR-swizzled
+        // by r % 8), once dV has read the dO tile there.
+        if (!(ok = warp_wait(&bars->dv_done[s], (i >> 1) & 1, wc))) break;
+        uint8_t* row = smem + C::kOffSlot + s * C::kSlotBytes + half * C::kDSChunk + r * 128;
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch)
             *reinterpret_cast<uint4*>(row + ((ch ^ (r & 7)) << 4)) =
@@ -358,6 +369,8 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&bars->ds_ready[half]);
+
+        if (i + 1 < Tq && !(ok = form_p(i + 1))) break;
 
         // dQ_i^T: this half's 64 query columns, thread = head-dimension index r.
         if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
@@ -370,8 +383,9 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         }
         tc_fence_before();
         mbar_arrive(&bars->dq_empty);
-        // Stage rows [HQ][D] (fp32): the step's Q tile (first half) or the second half's own buffer.
-        float* stage = reinterpret_cast<float*>(half == 0 ? smem + C::kOffQ + s * C::kQBytes : smem + C::kOffStageB);
+        // Stage rows [HQ][D] (fp32): the step's slot (dQ^T has read its dS^T) or the second half's buffer.
+        float* stage = reinterpret_cast<float*>(half == 0 ? smem + C::kOffSlot + s * C::kSlotBytes
+                                                          : smem + C::kOffStageB);
         // The second half's buffer is reused once the reduce of the previous step's rows has read it (it has
         // had a whole step); only the thread that issued that reduce can wait for it.
         if (half == 1 && i > 0) {
@@ -386,7 +400,7 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
             for (int q = 0; q < HQ; ++q) stage[q * D + r] = __uint_as_float(x[q / 32][q % 32]);
         }
         fence_proxy_async_smem();
-        mbar_arrive(half == 0 ? &bars->staged_q[s] : &bars->staged_b);
+        mbar_arrive(half == 0 ? &bars->staged_a[s] : &bars->staged_b);
         // The TMA thread reduces the first half; the second half's leader reduces its own.  A wait that
         // gives up has set the abort flag, which stops the whole warp at its next wait.
         if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
@@ -453,13 +467,12 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (threadIdx.x == 0) {
         bars->wait.budget = wait_budget;
         mbar_init(&bars->kv_full, 1);
-        for (int s = 0; s < kQStages; ++s) {
-            mbar_init(&bars->q_full[s], 1);
-            mbar_init(&bars->staged_q[s], 128);
-        }
         for (int t = 0; t < 2; ++t) {
+            mbar_init(&bars->q_full[t], 1);
+            mbar_init(&bars->q_empty[t], 1);
             mbar_init(&bars->do_full[t], 1);
-            mbar_init(&bars->do_empty[t], 1);
+            mbar_init(&bars->dv_done[t], 1);
+            mbar_init(&bars->staged_a[t], 128);
             mbar_init(&bars->p_ready[t], 128);
             mbar_init(&bars->ds_ready[t], 128);
         }
