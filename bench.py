@@ -202,6 +202,7 @@ def run_ours(args, w):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    launches0 = fa.fa_kernel_launches()
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xff)                      # evict the previous step's data from L2 (untimed)
@@ -214,6 +215,7 @@ def run_ours(args, w):
     if world > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - t_wall
+    launches = fa.fa_kernel_launches() - launches0          # counted by the library at each launch
     clk = clocks.stop()
     fa.fa_check_status(stream)
 
@@ -232,7 +234,6 @@ def run_ours(args, w):
 
     e2e_ms, h2d, d2h = _e2e(fa, w, inp_cpu, dev, args.steps)
     e2e_ms = max_over_ranks(e2e_ms, dev)
-    launches = _count_launches(step)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -244,8 +245,8 @@ def run_ours(args, w):
         "fwd_bwd_frac_of_peak": value / world / peak,
         "wall_s_timed_region": wall,
         "clocks": clk,
-        "gpu_launches": args.steps * launches["per_step"],
-        "gpu_launches_per_step": launches,
+        "gpu_launches": launches,
+        "gpu_launches_counted_by": "libfa.so's own launch counter (fa_kernel_launches) across the timed loop",
         "e2e": {"value": (w.fwd_flops() + w.bwd_flops()) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q,k,v,dO copied in and o,lse,dq,dk,dv copied out every step, through the "
@@ -253,6 +254,7 @@ def run_ours(args, w):
                        "transfers overlap steps i-1 and i+1's compute"},
     }
     line["roofline"] = _roofline(w, fwd_avg, bwd_avg, peaks)
+    line["exp_pipe"] = _exp_pipe(w, fwd_avg, bwd_avg)
     if rank == 0 and not args.no_cpu_baseline:
         f, t = _oracle_sample(w, args.oracle_heads, inp_cpu)
         meta = _cpu_meta(args.oracle_heads, w)
@@ -320,47 +322,24 @@ def _e2e(fa, w, inp_cpu, dev, steps):
     return start.elapsed_time(end) / steps, 4 * elt, 4 * elt + B * H * N * 4
 
 
-# Kernels launched per step when the profiler interface is unavailable: the forward's full waves and
-# its 2-CTA-cluster tail wave, and the backward's row-term, main and dQ kernels.
-LAUNCHES_PER_STEP_SCHEDULE = 5
-# Kernel names of libfa.so (they appear in both demangled and mangled profiler names).
-OUR_KERNELS = ("fwd_tc_kernel", "bwd_prep_kernel", "bwd_tc_kernel", "bwd_dq_convert_kernel", "fwd_simt_kernel")
-
-
-def _count_launches(step):
-    """Kernels of libfa.so launched by one (untimed) step, counted through the CUDA profiler interface
-    after every timed region has finished."""
-    if os.environ.get("FA_BENCH_NO_PROFILER") == "1":      # set when an outside profiler owns the counters
-        return {"per_step": LAUNCHES_PER_STEP_SCHEDULE, "counted_by": "schedule (FA_BENCH_NO_PROFILER=1)"}
-    try:
-        import tempfile
-        from torch.profiler import ProfilerActivity, profile
-        torch.cuda.synchronize()
-        with profile(activities=[ProfilerActivity.CPU, ProfilerActivity.CUDA]) as prof:
-            step()
-            torch.cuda.synchronize()
-        # Kernels launched straight through the library have no torch operator to hang on, so count the
-        # kernel records of the exported trace rather than the operator view.
-        with tempfile.TemporaryDirectory() as tmp:
-            path = os.path.join(tmp, "trace.json")
-            prof.export_chrome_trace(path)
-            with open(path) as f:
-                trace = json.load(f)
-        names = [e.get("name", "") for e in trace.get("traceEvents", []) if e.get("cat") == "kernel"]
-        mine = [n for n in names if any(k in n for k in OUR_KERNELS)]
-        ours = sorted({k for n in mine for k in OUR_KERNELS if k in n})
-        if mine:
-            return {"per_step": len(mine), "counted_by": "torch.profiler (CUPTI) kernel records, one untimed step",
-                    "kernels": ours}
-    except Exception as e:                                   # profiler interface missing on this host
-        return {"per_step": LAUNCHES_PER_STEP_SCHEDULE, "counted_by": f"schedule (profiler failed: {e})"}
-    return {"per_step": LAUNCHES_PER_STEP_SCHEDULE, "counted_by": "schedule (profiler saw no kernels)"}
-
-
 # DRAM bytes per launch of the dominant kernel at the bench workload, from one ncu capture of the
-# kernel as it is built now (profiles/dram_per_launch_bench_B1-H16-N8192-d128.md).  Set to None whenever
-# the kernel changes until it is measured again.
+# kernel as it is built now (dram__bytes_read.sum + dram__bytes_write.sum).  Set to None whenever the
+# kernel changes until it is measured again.
 TRAFFIC_BYTES = {("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): 202639616 + 83149056}
+
+
+# Measured throughput of the exponential unit (ex2.approx.f32, whole GPU), the second ceiling of the
+# softmax work: `python -m exact_io_aware_17_gb300.mufu_peak` on this GPU model.
+EX2_PER_S = 9.97e12
+
+
+def _exp_pipe(w, fwd_ms, bwd_ms):
+    """Exponentials per second of each pass against the measured ex2 throughput: B*H*N^2 exponentials in
+    the forward (P) and the same again in the backward (P recomputed)."""
+    n = w.B * w.H * w.N * w.N
+    fwd, bwd = n / (fwd_ms * 1e-3), n / (bwd_ms * 1e-3)
+    return {"unit": "ex2/s", "fwd": fwd, "bwd": bwd, "peak": EX2_PER_S, "frac_fwd": fwd / EX2_PER_S,
+            "frac_bwd": bwd / EX2_PER_S, "peak_source": "measured (ex2.approx throughput microbenchmark)"}
 
 
 def _roofline(w, fwd_ms, bwd_ms, peaks):

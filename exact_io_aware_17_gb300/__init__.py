@@ -20,7 +20,7 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3:
 
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc", "fa_last_error_string",
-           "fa_check_status")
+           "fa_check_status", "fa_kernel_launches")
 
 # Bytes of the static scratch that fa_bwd_noalloc uses (FA_BWD_NOALLOC_MAX_SCRATCH_BYTES).
 NOALLOC_MAX_SCRATCH_BYTES = 32 << 20
@@ -59,6 +59,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_last_error_string.restype = ctypes.c_char_p
     lib.fa_check_status.argtypes = [P]
     lib.fa_check_status.restype = I
+    lib.fa_kernel_launches.argtypes = []
+    lib.fa_kernel_launches.restype = ctypes.c_ulonglong
     _lib = lib
     return lib
 
@@ -170,10 +172,15 @@ def fa_check_status(stream=None):
     _check(load_library().fa_check_status(_stream(stream)))
 
 
+def fa_kernel_launches() -> int:
+    """Kernels libfa.so has launched in this process so far (a diagnostic; see include/fa.h)."""
+    return int(load_library().fa_kernel_launches())
+
+
 def fa_last_error_string() -> str:
     return load_library().fa_last_error_string().decode(errors="replace")
 
 
 __all__ = ["fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc", "fa_check_status",
            "fa_last_error_string",
-           "load_library", "FAError", "EXPORTS", "LIB_PATH"]
+           "fa_kernel_launches", "load_library", "FAError", "EXPORTS", "LIB_PATH"]

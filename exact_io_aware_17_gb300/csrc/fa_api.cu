@@ -3,6 +3,8 @@
 
 #include <cudaTypedefs.h>
 #include <math.h>
+
+#include <atomic>
 #include <stdlib.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -20,6 +22,12 @@ fa_status set_error(fa_status st, const char* fmt, ...) {
     va_end(ap);
     return st;
 }
+
+std::atomic<unsigned long long>& launch_counter() {
+    static std::atomic<unsigned long long> n{0};
+    return n;
+}
+void count_launches(int n) { launch_counter().fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
 static size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
@@ -105,6 +113,8 @@ using namespace fa;
 extern "C" {
 
 const char* fa_last_error_string(void) { return g_last_error; }
+
+unsigned long long fa_kernel_launches(void) { return fa::launch_counter().load(std::memory_order_relaxed); }
 
 static fa_status fwd_common(const char* fn, const void* q, const void* k, const void* v, void* o, float* lse, int B,
                             int H, int N, int d, float scale, void* stream, bool stepnorm) {

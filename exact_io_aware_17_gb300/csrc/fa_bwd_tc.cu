@@ -610,6 +610,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
                                                lse2, dq_acc, s.N, Npad, s.heads());
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    count_launches(1);
 
     CUtensorMap tq, tk, tv, tdo;
     if ((e = make_tmap_bf16_3d(&tq, q, s.d, s.N, s.heads(), BQ)) != cudaSuccess) return e;
@@ -625,8 +626,11 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
                                                             (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, s.N, Npad, bph, scale,
                                                             scale * 1.4426950408889634f, wait_policy().budget_cycles);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    count_launches(1);
     bwd_dq_convert_kernel<<<blocks, 256, 0, st>>>(dq_acc, (__nv_bfloat16*)dq, scale, s.heads() * (int64_t)s.N * D / 4);
-    return cudaGetLastError();
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    count_launches(1);
+    return cudaSuccess;
 }
 
 }  // namespace

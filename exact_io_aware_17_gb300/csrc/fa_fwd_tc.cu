@@ -534,6 +534,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
         fwd_tc_kernel<D, kStepNorm><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, out, lse, s.N, bph, 0, 0,
                                                                            scale_log2, wp.budget_cycles, wp.starve);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        count_launches(1);
     }
     if (split_tail) {
         cudaLaunchConfig_t cfg = {};
@@ -551,6 +552,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
         e = cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, kStepNorm>, tq, tk, tv, out, lse, s.N, bph, (int)full, 2,
                                scale_log2, wp.budget_cycles, wp.starve);
         if (e != cudaSuccess) return e;
+        count_launches(1);
     }
     return cudaGetLastError();
 }

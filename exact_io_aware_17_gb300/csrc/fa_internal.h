@@ -1,6 +1,7 @@
 // Host-side declarations shared by the translation units of libfa.so (no device code here).
 #pragma once
 
+#include <atomic>
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
@@ -56,5 +57,9 @@ cudaError_t launch_fwd_simt_f32(const float* q, const float* k, const float* v, 
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                           const float* lse, void* dq, void* dk, void* dv, const Shape& s, float scale,
                           void* workspace, cudaStream_t st);
+
+// Adds n to the process-wide count of kernels this library has launched (read by fa_kernel_launches).
+void count_launches(int n);
+std::atomic<unsigned long long>& launch_counter();
 
 }  // namespace fa

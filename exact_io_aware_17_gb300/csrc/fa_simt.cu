@@ -150,7 +150,9 @@ cudaError_t launch_fwd(const T* q, const T* k, const T* v, T* o, float* lse, con
     size_t smem = sizeof(float) * (2 * kBlk * (s.d + 1) + kWarps * kRows * s.d);
     cudaFuncSetAttribute(fwd_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     fwd_simt_kernel<T><<<grid, kWarps * 32, smem, st>>>(q, k, v, o, lse, s.N, s.d, bph, scale);
-    return cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) count_launches(1);
+    return e;
 }
 
 }  // namespace

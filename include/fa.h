@@ -131,6 +131,14 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
 const char* fa_last_error_string(void);
 
 /*
+ * fa_kernel_launches — number of kernels this library has launched in this process so far, over all
+ * threads and devices; every entry point adds each kernel it enqueues (fa_fwd: one or two, the second for
+ * the last partial wave of tiles; fa_bwd: three; fa_fwd_f32: one).  Never reset.  A diagnostic: the
+ * difference across a region counts the launches made in it.
+ */
+unsigned long long fa_kernel_launches(void);
+
+/*
  * fa_check_status — synchronises `stream`, then reports and clears the device status word:
  * FA_ERR_TIMEOUT if a kernel gave up a bounded wait since the last check, FA_ERR_CUDA if the stream
  * reported an error, else FA_OK.  A debugging and test helper; the fast path never calls it.

@@ -117,3 +117,12 @@ def test_error_string_is_replaced_by_the_next_failure(fa):
     assert "B, H, N, d must be >= 1" in fa.fa_last_error_string()
     _fwd(lib, d=32)
     assert "d must be 64 or 128" in fa.fa_last_error_string()
+
+
+def test_kernel_launch_counter_counts_nothing_without_launches(fa):
+    """fa_kernel_launches counts enqueued kernels only: calls rejected before any launch leave it alone."""
+    before = fa.fa_kernel_launches()
+    assert before >= 0
+    lib = fa.load_library()
+    assert lib.fa_fwd(None, None, None, None, None, 1, 1, 8, 64, 0.125, None) == 1   # FA_ERR_INVALID_ARG
+    assert fa.fa_kernel_launches() == before

@@ -150,3 +150,40 @@ def test_bwd_more_heads_than_a_grid_dimension_holds():
     rq, rk, rv = oracle.backward(*(np64(t) for t in sub), 0.125)
     for g, r in ((dq, rq), (dk, rk), (dv, rv)):
         assert rel_fro(np64(g.reshape(B * H, N, d)[sel]), r[0]) <= TOL_GRAD_BF16
+
+
+def test_bwd_allocates_nothing_with_caller_buffers():
+    """With every output and the workspace owned by the caller, fa_bwd allocates no device memory at all;
+    the workspace itself is O(B*H*N*d) (one fp32 score matrix at this shape would be 67 MB per head)."""
+    fa = need_gpu()
+    B, H, N, d = 1, 4, 4096, 128
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed=731, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fa_fwd(q, k, v, 1 / math.sqrt(d))
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device="cuda")
+    assert ws.numel() < 2 * B * H * N * (d + 2) * 4 + 4096
+    torch.cuda.synchronize()
+    torch.cuda.reset_peak_memory_stats()
+    before = torch.cuda.memory_allocated()
+    fa.fa_bwd(q, k, v, o, do, lse, 1 / math.sqrt(d), dq, dk, dv, ws)
+    torch.cuda.synchronize()
+    fa.fa_check_status()
+    assert torch.cuda.max_memory_allocated() == before
+
+
+def test_kernel_launch_counter_per_call():
+    """The library counts its own launches: fa_fwd enqueues one kernel, or two when the last partial wave
+    of tile pairs runs as 2-CTA clusters; fa_bwd enqueues three (row terms, main, dQ conversion)."""
+    fa = need_gpu()
+    inp = fa_inputs.make_inputs(1, 4, 1024, 128, "bf16", seed=77, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    n0 = fa.fa_kernel_launches()
+    o, lse = fa.fa_fwd(q, k, v, 0.088)
+    n1 = fa.fa_kernel_launches()
+    fa.fa_bwd(q, k, v, o, do, lse, 0.088)
+    n2 = fa.fa_kernel_launches()
+    torch.cuda.synchronize()
+    fa.fa_check_status()
+    assert n1 - n0 in (1, 2)
+    assert n2 - n1 == 3
