@@ -64,7 +64,7 @@ cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, 
 
 WaitPolicy wait_policy() {
     const char* v = getenv("FA_TEST_STARVE_WAIT");
-    if (v && v[0] == '1') return WaitPolicy{20000000LL, 1};  // ~10 ms, and the forward's Q loads withheld
+    if (v && v[0] == '1') return WaitPolicy{20000000LL, 1};  // ~10 ms, and the kernels' Q loads withheld
     return WaitPolicy{4000000000LL, 0};                       // ~2 s: no legitimate wait comes near it
 }
 

@@ -130,7 +130,7 @@ template <int D>
 __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
                              const CUtensorMap* tm_do, const float* lse2, const float* row_d,
                              float* __restrict__ dq_acc, uint8_t* smem, BwdBarriers* bars, int head, int k0, int N,
-                             int Tq, int Npad, int rot) {
+                             int Tq, int Npad, int rot, int starve) {
     using C = BwdCfg<D>;
     WaitCtl* wc = &bars->wait;
     const uint64_t pol_keep = policy_evict_last();
@@ -159,15 +159,20 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         const int s = i & 1;
         const int qb = qblock(i, rot, Tq);
         if (i >= 2 && !(ok = mbar_wait(&bars->q_empty[s], ((i >> 1) - 1) & 1, wc))) break;
-        uint64_t* bar = &bars->q_full[s];
-        mbar_expect_tx(bar, C::kQBytes + 2 * C::kRowBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem + C::kOffQ + s * C::kQBytes + c * C::kChunkQ, tm_q, bar, c * 64, qb * BQ, head, pol_keep);
-        float* rows = reinterpret_cast<float*>(smem + C::kOffRows) + s * 2 * BQ;
-        const size_t r0 = (size_t)head * Npad + (size_t)qb * BQ;
-        bulk_load(rows, lse2 + r0, C::kRowBytes, bar);
-        bulk_load(rows + BQ, row_d + r0, C::kRowBytes, bar);
-        q_issued = i + 1;
+        // starve != 0 withholds the Q loads so that the first waits on them run out: the failure path of
+        // the bounded waits, exercised by the tests with a short budget.
+        if (!starve) {
+            uint64_t* bar = &bars->q_full[s];
+            mbar_expect_tx(bar, C::kQBytes + 2 * C::kRowBytes);
+            for (int c = 0; c < C::kChunks; ++c)
+                tma_load_3d(smem + C::kOffQ + s * C::kQBytes + c * C::kChunkQ, tm_q, bar, c * 64, qb * BQ, head,
+                            pol_keep);
+            float* rows = reinterpret_cast<float*>(smem + C::kOffRows) + s * 2 * BQ;
+            const size_t r0 = (size_t)head * Npad + (size_t)qb * BQ;
+            bulk_load(rows, lse2 + r0, C::kRowBytes, bar);
+            bulk_load(rows + BQ, row_d + r0, C::kRowBytes, bar);
+            q_issued = i + 1;
+        }
 
         if (i >= 2) {
             if (!(ok = reduce_first_half(i - 2))) break;
@@ -445,7 +450,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
               const float* __restrict__ lse2, const float* __restrict__ row_d, float* __restrict__ dq_acc,
               __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int N, int Npad,
-              int blocks_per_head, float scale, float scale_log2, long long wait_budget) {
+              int blocks_per_head, float scale, float scale_log2, long long wait_budget, int starve) {
     using C = BwdCfg<D>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t pad = (1024 - (smem_u32(smem_raw) & 1023)) & 1023;
@@ -509,7 +514,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     if (warp == kTmaWarp) {
         if (lane == 0)
-            bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, lse2, row_d, dq_acc, smem, bars, head, k0, N, Tq, Npad, rot);
+            bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, lse2, row_d, dq_acc, smem, bars, head, k0, N, Tq, Npad, rot,
+                            starve);
     } else if (warp == kMmaWarp) {
         if (lane == 0) bwd_mma<D>(smem, bars, tmem, Tq);
     } else {
@@ -622,9 +628,10 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     const int bph = (s.N + BK - 1) / BK;
     if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
     const unsigned grid = (unsigned)(bph * s.heads());
+    const WaitPolicy wp = wait_policy();
     bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, lse2, row_d, dq_acc,
                                                             (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, s.N, Npad, bph, scale,
-                                                            scale * 1.4426950408889634f, wait_policy().budget_cycles);
+                                                            scale * 1.4426950408889634f, wp.budget_cycles, wp.starve);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     count_launches(1);
     bwd_dq_convert_kernel<<<blocks, 256, 0, st>>>(dq_acc, (__nv_bfloat16*)dq, scale, s.heads() * (int64_t)s.N * D / 4);

@@ -1,9 +1,10 @@
 """Failure detection of the bounded device waits (GPU; no fault, trap or hang).
 
-With FA_TEST_STARVE_WAIT=1 in the environment the forward withholds its Q loads and its waits get a
-~10 ms budget, so the MMA warp's first wait runs out: the kernel must wind down by itself (the other
-warps stop at their next wait, tensor memory is freed) and fa_check_status must report FA_ERR_TIMEOUT.
-The CUDA context must stay usable: the next call with the switch off computes correct results."""
+With FA_TEST_STARVE_WAIT=1 in the environment the forward and backward kernels withhold their Q loads and
+their waits get a ~10 ms budget, so the MMA warp's first wait on Q runs out: the kernel must wind down
+by itself (the other warps stop at their next wait, copies in flight land, tensor memory is freed) and
+fa_check_status must report FA_ERR_TIMEOUT.  The CUDA context must stay usable: the next call with the
+switch off computes correct results."""
 import math
 
 import pytest
@@ -11,7 +12,7 @@ import torch
 
 import fa_inputs
 import oracle
-from parity_util import TOL_LSE_BF16, TOL_O_BF16, max_abs, need_gpu, np64
+from parity_util import TOL_GRAD_BF16, TOL_LSE_BF16, TOL_O_BF16, max_abs, need_gpu, np64, rel_fro
 
 pytestmark = pytest.mark.gpu
 
@@ -36,3 +37,27 @@ def test_forward_wait_that_runs_out_reports_timeout(monkeypatch):
     ro, rl = oracle.forward(np64(inp["q"]), np64(inp["k"]), np64(inp["v"]), scale)
     assert max_abs(np64(o), ro) <= TOL_O_BF16
     assert max_abs(np64(lse), rl) <= TOL_LSE_BF16
+
+
+def test_backward_wait_that_runs_out_reports_timeout(monkeypatch):
+    fa = need_gpu()
+    B, H, N, d = 1, 2, 300, 64
+    scale = 1 / math.sqrt(d)
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed=78, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fa_fwd(q, k, v, scale)
+    torch.cuda.synchronize()
+    fa.fa_check_status()                                  # start from a clear status word
+    monkeypatch.setenv("FA_TEST_STARVE_WAIT", "1")
+    fa.fa_bwd(q, k, v, o, do, lse, scale)
+    with pytest.raises(fa.FAError) as err:
+        fa.fa_check_status()
+    assert err.value.status == fa.FA_ERR_TIMEOUT
+    monkeypatch.delenv("FA_TEST_STARVE_WAIT")
+    fa.fa_check_status()
+    dq, dk, dv = fa.fa_bwd(q, k, v, o, do, lse, scale)
+    torch.cuda.synchronize()
+    fa.fa_check_status()
+    rq, rk, rv = oracle.backward(*(np64(inp[n]) for n in ("q", "k", "v", "do")), scale)
+    errs = rel_fro(np64(dq), rq), rel_fro(np64(dk), rk), rel_fro(np64(dv), rv)
+    assert max(errs) <= TOL_GRAD_BF16, errs
