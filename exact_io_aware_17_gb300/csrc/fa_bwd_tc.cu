@@ -380,12 +380,11 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         // dQ_i^T: this half's 64 query columns, thread = head-dimension index r.
         if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
         tc_fence_after();
+        // Every warp loads (lanes >= D hold the d = 64 padding rows, which are not staged).
         uint32_t x[2][32];
-        if (dq_lane) {
-            tmem_ld32(tmem + lane_off + C::kColDP + half * HQ, x[0]);
-            tmem_ld32(tmem + lane_off + C::kColDP + half * HQ + 32, x[1]);
-            tmem_ld_wait();
-        }
+        tmem_ld32(tmem + lane_off + C::kColDP + half * HQ, x[0]);
+        tmem_ld32(tmem + lane_off + C::kColDP + half * HQ + 32, x[1]);
+        tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&bars->dq_empty);
         // Stage rows [HQ][D] (fp32): the step's slot (dQ^T has read its dS^T) or the second half's buffer.

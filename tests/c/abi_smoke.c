@@ -78,12 +78,16 @@ int main(void) {
     for (int t = 0; t < 4; ++t) CHECK_CUDA(cudaMemcpy(dev_b[t], hb[t], n * 2, cudaMemcpyHostToDevice));
     for (int t = 0; t < 3; ++t) CHECK_CUDA(cudaMemcpy(dev_f[t], hf[t], n * 4, cudaMemcpyHostToDevice));
 
+    const unsigned long long launches0 = fa_kernel_launches();
     if (fa_fwd(q, k, v, o, lse, B, H, N, d, scale, NULL) != FA_OK) { fprintf(stderr, "fa_fwd: %s\n", fa_last_error_string()); return 1; }
     if (fa_fwd_f32(qf, kf, vf, of, lsef, B, H, N, d, scale, NULL) != FA_OK) { fprintf(stderr, "fa_fwd_f32: %s\n", fa_last_error_string()); return 1; }
     const size_t wsb = fa_bwd_workspace_size(B, H, N, d);
     CHECK_CUDA(cudaMalloc(&ws, wsb));
     if (fa_bwd(q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, ws, wsb, NULL) != FA_OK) { fprintf(stderr, "fa_bwd: %s\n", fa_last_error_string()); return 1; }
     if (fa_check_status(NULL) != FA_OK) { fprintf(stderr, "status: %s\n", fa_last_error_string()); return 1; }
+    /* fa_fwd: one or two kernels, fa_fwd_f32: one, fa_bwd: three. */
+    const unsigned long long launches = fa_kernel_launches() - launches0;
+    if (launches < 5 || launches > 6) { fprintf(stderr, "kernel launches: %llu\n", launches); return 1; }
 
     uint16_t* ho = malloc(n * 2);
     float *hof = malloc(n * 4), *hl = malloc(rows * 4), *hlf = malloc(rows * 4);
