@@ -27,18 +27,22 @@
 // Every product is 128 x 128 x 128 (M = 128 keys or head dimensions, N = 128 queries or head
 // dimensions): N = 128 is the narrowest tcgen05 shape that runs at the full rate, which 64-query steps
 // (three of five products at N = 64) did not reach.  Tensor memory then holds exactly S^T, dP^T, dV and
-// dK (4 x 128 columns at d = 128), with dQ^T reusing the columns of dP^T.  S^T of the next step is issued
-// right behind dQ^T, so moving dQ^T out of tensor memory overlaps the next S^T.
+// dK (4 x 128 columns at d = 128), with dQ^T reusing the columns of dP^T.  The MMAs of step i run in the
+// order dV(i), S^T(i+1), dK(i), dQ^T(i), dP^T(i+1): the next S^T goes right behind dV (its columns held
+// P^T, which dV has just read), so forming P(i+1) overlaps dK and dQ^T on the tensor core.
 //
 // Warp roles (320 threads): warps 0-3 and 4-7 are two warpgroups that own the same 128 key rows
 // (tensor-memory lanes) and split each step's queries, 64 each: they form P^T and dS^T for their half,
-// then move their half of dQ_i^T out of tensor memory (thread = head-dimension index) and issue its
-// reduce-add, and at the end write dV (warps 0-3) and dK (warps 4-7).  Warp 8 issues TMA loads, warp 9
-// allocates tensor memory and issues the MMAs.
+// then move their half of dQ_i^T out of tensor memory (thread = head-dimension index) and stage it, and
+// at the end write dV (warps 0-3) and dK (warps 4-7).  Warp 8 issues the TMA loads and the first half's
+// reduce-adds, warp 9 allocates tensor memory and issues the MMAs; the second half's reduce-adds come
+// from its own leader thread.
 //
-// Shared memory (d = 128: 226 KB) has one dQ staging buffer: the first half's dQ rows are staged in the
-// Q tile of the step (no longer read once dK has been formed), which the TMA thread adds into the
-// accumulator and then reloads; the second half's rows have a buffer of their own.
+// Shared memory (d = 128: 226 KB): K and V resident, two Q stages, and two slots that each hold a step's dO
+// tile, then its dS^T (once dV has read dO), then the first half's fp32 dQ rows (once dQ^T has read dS^T);
+// the TMA thread adds those rows into the accumulator and loads the dO tile of step i + 2 there.  The
+// second half's dQ rows have a buffer of their own.  The kernel has no static shared memory, so its
+// dynamic region starts aligned and needs no slack.
 //
 // For d = 64 the dQ^T product still uses M = 128: the A operand's second 64-row half points at a
 // zeroed shared-memory block, and the rows it produces are ignored.
