@@ -119,6 +119,11 @@ struct BwdCfg {
     static constexpr uint32_t kAlignSlack = kSmemNeed + 1024 <= 232448 ? 1024 : 232448 - kSmemNeed;
     static constexpr uint32_t kSmemBytes = kSmemNeed + kAlignSlack;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
+    // dQ^T reuses the columns of dP^T at d = 128 (all 512 are taken); at d = 64 it has 128 spare columns
+    // of its own, so the next dP^T need not wait for it to be moved out.
+    static constexpr bool kOwnDQ = D == 64;
+    static constexpr uint32_t kColDQ = kOwnDQ ? 256 + 2 * D : kColDP;
+    static_assert(kColDQ + 128 <= 512, "tensor memory columns");
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kQBytes <= kSlotBytes && kHalfDQBytes <= kSlotBytes, "slot contents");
     static_assert(kSmemNeed <= 232448, "shared memory per CTA");
@@ -234,9 +239,10 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
             mma_ts(d, a + kk * 8, sdesc_advance(b0, (half * (HQ / 16) + kk) * 16 * 128), idG,
                    (acc || kk > 0) ? 1u : 0u);
     };
-    // dQ^T = K^T dS^T over the 128 keys, into the columns of dP^T (free once dK used dS^T).
+    // dQ^T = K^T dS^T over the 128 keys, into the columns of dP^T (free once dK used dS^T) or, at d = 64,
+    // into columns of its own.
     auto dq = [&](uint64_t b0) {
-        const uint32_t d = tmem + C::kColDP;
+        const uint32_t d = tmem + C::kColDQ;
 #pragma unroll
         for (int kk = 0; kk < BK / 16; ++kk)
             mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(b0, kk * 16 * 128), idQ, kk > 0);
@@ -276,12 +282,14 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         }
         if (!ok) break;
         mma_commit(&bars->q_empty[s]);
+        // At d = 64 dQ^T has its own columns, which dQ^T of step i-1 must have left.
+        if (C::kOwnDQ && i > 0 && !(ok = mbar_wait_poll(&bars->dq_empty, (i - 1) & 1, wc))) break;
         dq(sdesc_advance(mDS, s * C::kSlotBytes));
         mma_commit(&bars->dq_full);
         if (i + 1 < Tq) {
             if (!(ok = mbar_wait_poll(&bars->do_full[s1], ((i + 1) >> 1) & 1, wc))) break;
-            // The columns of dP^T hold dQ^T of step i until it has been moved out.
-            if (!(ok = mbar_wait_poll(&bars->dq_empty, i & 1, wc))) break;
+            // At d = 128 the columns of dP^T hold dQ^T of step i until it has been moved out.
+            if (!C::kOwnDQ && !(ok = mbar_wait_poll(&bars->dq_empty, i & 1, wc))) break;
             tc_fence_after();
             qk_like(kV, sdesc_advance(kDO, s1 * C::kSlotBytes), C::kColDP);
             mma_commit(&bars->dp_full);
@@ -386,8 +394,8 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         tc_fence_after();
         // Every warp loads (lanes >= D hold the d = 64 padding rows, which are not staged).
         uint32_t x[2][32];
-        tmem_ld32(tmem + lane_off + C::kColDP + half * HQ, x[0]);
-        tmem_ld32(tmem + lane_off + C::kColDP + half * HQ + 32, x[1]);
+        tmem_ld32(tmem + lane_off + C::kColDQ + half * HQ, x[0]);
+        tmem_ld32(tmem + lane_off + C::kColDQ + half * HQ + 32, x[1]);
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&bars->dq_empty);
