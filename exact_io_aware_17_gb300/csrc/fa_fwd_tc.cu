@@ -60,9 +60,10 @@ struct FwdBarriers {
     uint64_t k_full[kMaxStages];
     uint64_t v_full[kMaxStages];
     uint64_t kv_empty[kMaxStages];
-    uint64_t s_full[2];
-    uint64_t p_full[2];
+    uint64_t s_full[2][2];   // [tile][block parity]: S of a tile's block j is in TMEM
+    uint64_t p_full[2][2];   // [tile][block parity]: P of a tile's block j is in TMEM
     uint64_t o_full[2];
+    uint64_t pv_done[2];   // d = 64: PV of a tile has completed (before its accumulator may be rescaled)
     uint64_t mma_done;
     uint32_t tmem_base;
     WaitCtl wait;
@@ -81,8 +82,14 @@ struct FwdCfg {
     static constexpr uint32_t kOffV = kOffK + kStages * kKVBytes;
     static constexpr uint32_t kOffBar = kOffV + kStages * kKVBytes;
     static constexpr uint32_t kSmemBytes = kOffBar + sizeof(FwdBarriers) + 1024;  // + alignment slack
+    // d = 64 leaves room for a third S buffer: S tiles rotate through three buffers (S of block j + 1 is
+    // formed while the softmax of block j runs) and O0, O1 take the last 128 columns.  At d = 128 each
+    // tile has one S buffer.
+    static constexpr bool kThreeS = D == 64;
     __host__ __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 128; }
-    __host__ __device__ static constexpr uint32_t col_o(int t) { return 256 + (uint32_t)t * D; }
+    __host__ __device__ static constexpr uint32_t col_o(int t) { return (kThreeS ? 384 : 256) + (uint32_t)t * D; }
+    // Buffer of the S tile with issue index k = 2 j + t (block j, tile t) when there are three.
+    __host__ __device__ static constexpr uint32_t col_s3(int k) { return (uint32_t)(k % 3) * 128; }
     static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -135,41 +142,82 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
     const uint64_t dK0 = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t dV0 = sdesc_sw128(smem_u32(smem + C::kOffV), C::kChunkKV, 1024);
 
-    auto issue_s = [&](int t, int s) {
+    auto issue_s_to = [&](int t, int s, uint32_t col) {
         const uint64_t a0 = sdesc_advance(dQ0, t * C::kQBytes);
         const uint64_t b0 = sdesc_advance(dK0, s * C::kKVBytes);
-        const uint32_t d = tmem + C::col_s(t);
+        const uint32_t d = tmem + col;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
             mma_ss(d, sdesc_advance(a0, (kk / 4) * C::kChunkQ + (kk % 4) * 32),
                    sdesc_advance(b0, (kk / 4) * C::kChunkKV + (kk % 4) * 32), idS, kk > 0);
         }
     };
-    auto issue_pv = [&](int t, int s, bool accumulate) {
+    auto issue_s = [&](int t, int s) { issue_s_to(t, s, C::col_s(t)); };
+    auto issue_pv_from = [&](int t, int s, bool accumulate, uint32_t col) {
         const uint64_t b0 = sdesc_advance(dV0, s * C::kKVBytes);
         const uint32_t d = tmem + C::col_o(t);
-        const uint32_t a = tmem + C::col_s(t);
+        const uint32_t a = tmem + col;
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk)
             mma_ts(d, a + kk * 8, sdesc_advance(b0, kk * 16 * 128), idPV, (accumulate || kk > 0) ? 1u : 0u);
     };
+    auto issue_pv = [&](int t, int s, bool accumulate) { issue_pv_from(t, s, accumulate, C::col_s(t)); };
 
     bool ok = mbar_wait_poll(&bars->q_full[0], 0, wc) && mbar_wait_poll(&bars->q_full[1], 0, wc);
-    for (int j = 0; ok && j < T; ++j) {
+    if constexpr (C::kThreeS) {
+        // S tiles in issue order k = 2 j + t go to buffer k % 3; PV(k) frees that buffer for S(k + 3), so
+        // S of the next block is ready when the softmax warps finish the current one.
+        auto kwait = [&](int j) {
+            return mbar_wait_poll(&bars->k_full[j % C::kStages], (j / C::kStages) & 1, wc);
+        };
+        if (ok && (ok = kwait(0))) {
+            tc_fence_after();
+            issue_s_to(0, 0, C::col_s3(0));
+            mma_commit(&bars->s_full[0][0]);
+            issue_s_to(1, 0, C::col_s3(1));
+            mma_commit(&bars->s_full[1][0]);
+            if (T > 1 && (ok = kwait(1))) {
+                tc_fence_after();
+                issue_s_to(0, 1 % C::kStages, C::col_s3(2));
+                mma_commit(&bars->s_full[0][1]);
+            }
+        }
+        for (int j = 0; ok && j < T; ++j) {
+            const int s = j % C::kStages;
+            if (!(ok = mbar_wait_poll(&bars->v_full[s], (j / C::kStages) & 1, wc))) break;
+            for (int t = 0; ok && t < 2; ++t) {
+                const int k = 2 * j + t;
+                if (!(ok = mbar_wait_poll(&bars->p_full[t][j & 1], (j >> 1) & 1, wc))) break;
+                tc_fence_after();
+                issue_pv_from(t, s, j > 0, C::col_s3(k));
+                mma_commit(&bars->pv_done[t]);
+                if (j == T - 1) mma_commit(&bars->o_full[t]);
+                if (t == 1) mma_commit(&bars->kv_empty[s]);
+                const int kn = k + 3, jn = kn / 2, tn = kn % 2;
+                if (jn < T) {
+                    if (tn == 0 && !(ok = kwait(jn))) break;
+                    tc_fence_after();
+                    issue_s_to(tn, jn % C::kStages, C::col_s3(kn));
+                    mma_commit(&bars->s_full[tn][jn & 1]);
+                }
+            }
+        }
+    }
+    for (int j = 0; !C::kThreeS && ok && j < T; ++j) {
         const int s = j % C::kStages;
         const uint32_t ph = (j / C::kStages) & 1;
         if (j == 0) {
             if (!(ok = mbar_wait_poll(&bars->k_full[s], ph, wc))) break;
             tc_fence_after();
             issue_s(0, s);
-            mma_commit(&bars->s_full[0]);
+            mma_commit(&bars->s_full[0][0]);
             issue_s(1, s);
-            mma_commit(&bars->s_full[1]);
+            mma_commit(&bars->s_full[1][0]);
         }
         const int s2 = (j + 1) % C::kStages;
         const uint32_t ph2 = ((j + 1) / C::kStages) & 1;
         if (!(ok = mbar_wait_poll(&bars->v_full[s], ph, wc))) break;
-        if (!(ok = mbar_wait_poll(&bars->p_full[0], j & 1, wc))) break;
+        if (!(ok = mbar_wait_poll(&bars->p_full[0][j & 1], (j >> 1) & 1, wc))) break;
         tc_fence_after();
         issue_pv(0, s, j > 0);
         if (j == T - 1) mma_commit(&bars->o_full[0]);
@@ -177,16 +225,16 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
             if (!(ok = mbar_wait_poll(&bars->k_full[s2], ph2, wc))) break;
             tc_fence_after();
             issue_s(0, s2);
-            mma_commit(&bars->s_full[0]);
+            mma_commit(&bars->s_full[0][(j + 1) & 1]);
         }
-        if (!(ok = mbar_wait_poll(&bars->p_full[1], j & 1, wc))) break;
+        if (!(ok = mbar_wait_poll(&bars->p_full[1][j & 1], (j >> 1) & 1, wc))) break;
         tc_fence_after();
         issue_pv(1, s, j > 0);
         mma_commit(&bars->kv_empty[s]);
         if (j == T - 1) mma_commit(&bars->o_full[1]);
         if (j + 1 < T) {
             issue_s(1, s2);
-            mma_commit(&bars->s_full[1]);
+            mma_commit(&bars->s_full[1][(j + 1) & 1]);
         }
     }
     // Tensor memory is freed after this: every MMA issued must have completed.
@@ -203,15 +251,16 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
     const int quarter = warp & 3;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
-    const uint32_t tS = tmem + C::col_s(t) + lane_off;
+    const uint32_t tS1 = tmem + C::col_s(t) + lane_off;
     const uint32_t tO = tmem + C::col_o(t) + lane_off;
     const int tail = N - (T_all - 1) * BN;  // valid keys in the head's last block (1..BN)
 
     float m_run = -INFINITY, l_run = 0.f;
     bool ok = true;
     for (int j = 0; j < T; ++j) {
-        if (!(ok = warp_wait(&bars->s_full[t], j & 1, wc))) break;
+        if (!(ok = warp_wait(&bars->s_full[t][j & 1], (j >> 1) & 1, wc))) break;
         tc_fence_after();
+        const uint32_t tS = C::kThreeS ? tmem + C::col_s3(2 * j + t) + lane_off : tS1;
         uint32_t r[4][32];
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, r[q]);
@@ -266,6 +315,8 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
                 }
                 tmem_st32(tS + h * 32, pk);
             }
+            // With three S buffers, PV of the previous block may still be accumulating into O.
+            if (C::kThreeS && j > 0 && !(ok = warp_wait(&bars->pv_done[t], (j - 1) & 1, wc))) break;
             if (j > 0) {
                 const float c_old = alpha * l_run * inv;
 #pragma unroll
@@ -281,7 +332,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
             l_run = l_new;
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&bars->p_full[t]);
+            mbar_arrive(&bars->p_full[t][j & 1]);
             continue;
         }
         const float m_new = fmaxf(m_run, mx * scale_log2);
@@ -316,6 +367,8 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
         const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
         l_run = l_run * alpha + sum;
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+            // With three S buffers, PV of the previous block may still be accumulating into O.
+            if (C::kThreeS && !(ok = warp_wait(&bars->pv_done[t], (j - 1) & 1, wc))) break;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t x[32];
@@ -328,7 +381,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(&bars->p_full[t]);
+        mbar_arrive(&bars->p_full[t][j & 1]);
     }
     if (!ok) return;
     if (!warp_wait(&bars->o_full[t], 0, wc)) return;
@@ -451,9 +504,12 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         bars->wait.budget = wait_budget;
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->q_full[t], 1);
-            mbar_init(&bars->s_full[t], 1);
-            mbar_init(&bars->p_full[t], BM);
+            for (int b = 0; b < 2; ++b) {
+                mbar_init(&bars->s_full[t][b], 1);
+                mbar_init(&bars->p_full[t][b], BM);
+            }
             mbar_init(&bars->o_full[t], 1);
+            mbar_init(&bars->pv_done[t], 1);
         }
         for (int s = 0; s < kMaxStages; ++s) {
             mbar_init(&bars->k_full[s], 1);
