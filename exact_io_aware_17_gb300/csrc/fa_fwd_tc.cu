@@ -63,7 +63,7 @@ struct FwdBarriers {
     uint64_t s_full[2][2];   // [tile][block parity]: S of a tile's block j is in TMEM
     uint64_t p_full[2][2];   // [tile][block parity]: P of a tile's block j is in TMEM
     uint64_t o_full[2];
-    uint64_t pv_done[2];   // d = 64: PV of a tile has completed (before its accumulator may be rescaled)
+    uint64_t pv_done[2];   // d = 64, per-step normalisation: PV of a tile has completed (before O is rescaled)
     uint64_t mma_done;
     uint32_t tmem_base;
     WaitCtl wait;
@@ -86,6 +86,9 @@ struct FwdCfg {
     // formed while the softmax of block j runs) and O0, O1 take the last 128 columns.  At d = 128 each
     // tile has one S buffer.
     static constexpr bool kThreeS = D == 64;
+    // d = 64 keeps four K/V stages, so a block's V has long landed when its K is waited for: one barrier per
+    // stage covers both, which spares the MMA thread one barrier test per block.
+    static constexpr bool kOneKVBarrier = D == 64;
     __host__ __device__ static constexpr uint32_t col_s(int t) { return (uint32_t)t * 128; }
     __host__ __device__ static constexpr uint32_t col_o(int t) { return (kThreeS ? 384 : 256) + (uint32_t)t * D; }
     // Buffer of the S tile with issue index k = 2 j + t (block j, tile t) when there are three.
@@ -112,13 +115,15 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
     for (int j = 0; j < T; ++j) {
         const int s = j % C::kStages;
         if (j >= C::kStages && !mbar_wait(&bars->kv_empty[s], ((j / C::kStages) - 1) & 1, wc)) break;
-        mbar_expect_tx(&bars->k_full[s], C::kKVBytes);
+        // With one K/V barrier (d = 64) both tiles complete on k_full.
+        uint64_t* v_bar = C::kOneKVBarrier ? &bars->k_full[s] : &bars->v_full[s];
+        mbar_expect_tx(&bars->k_full[s], C::kOneKVBarrier ? 2 * C::kKVBytes : C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
             tma_load_3d(smem + C::kOffK + s * C::kKVBytes + c * C::kChunkKV, tm_k, &bars->k_full[s], c * 64,
                         (kv0 + j) * BN, head, pol_kv);
-        mbar_expect_tx(&bars->v_full[s], C::kKVBytes);
+        if (!C::kOneKVBarrier) mbar_expect_tx(v_bar, C::kKVBytes);
         for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem + C::kOffV + s * C::kKVBytes + c * C::kChunkKV, tm_v, &bars->v_full[s], c * 64,
+            tma_load_3d(smem + C::kOffV + s * C::kKVBytes + c * C::kChunkKV, tm_v, v_bar, c * 64,
                         (kv0 + j) * BN, head, pol_kv);
         issued = j + 1;
     }
@@ -127,11 +132,11 @@ __device__ void producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const
     drain_wait(&bars->q_full[1], 0, wc);
     for (int j = (issued > C::kStages ? issued - C::kStages : 0); j < issued; ++j) {
         drain_wait(&bars->k_full[j % C::kStages], (j / C::kStages) & 1, wc);
-        drain_wait(&bars->v_full[j % C::kStages], (j / C::kStages) & 1, wc);
+        if (!C::kOneKVBarrier) drain_wait(&bars->v_full[j % C::kStages], (j / C::kStages) & 1, wc);
     }
 }
 
-template <int D>
+template <int D, bool kStepNorm>
 __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int T) {
     using C = FwdCfg<D>;
     WaitCtl* wc = &bars->wait;
@@ -182,15 +187,18 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
                 mma_commit(&bars->s_full[0][1]);
             }
         }
+        // V of block j shares K's barrier, which kwait(j) saw before S of block j was issued.
+        static_assert(C::kOneKVBarrier, "the three-buffer loop relies on one K/V barrier per stage");
         for (int j = 0; ok && j < T; ++j) {
             const int s = j % C::kStages;
-            if (!(ok = mbar_wait_poll(&bars->v_full[s], (j / C::kStages) & 1, wc))) break;
             for (int t = 0; ok && t < 2; ++t) {
                 const int k = 2 * j + t;
                 if (!(ok = mbar_wait_poll(&bars->p_full[t][j & 1], (j >> 1) & 1, wc))) break;
                 tc_fence_after();
                 issue_pv_from(t, s, j > 0, C::col_s3(k));
-                mma_commit(&bars->pv_done[t]);
+                // Only the per-step normalisation rescales O on every block; the lazy rescale finds PV(k)
+                // complete through a later commit (see prev_pv_done in the softmax warps).
+                if (kStepNorm) mma_commit(&bars->pv_done[t]);
                 if (j == T - 1) mma_commit(&bars->o_full[t]);
                 if (t == 1) mma_commit(&bars->kv_empty[s]);
                 const int kn = k + 3, jn = kn / 2, tn = kn % 2;
@@ -240,6 +248,23 @@ __device__ void mma_issuer(uint8_t* smem, FwdBarriers* bars, uint32_t tmem, int 
     // Tensor memory is freed after this: every MMA issued must have completed.
     mma_commit(&bars->mma_done);
     drain_wait(&bars->mma_done, 0, wc);
+}
+
+// Three S buffers, lazy rescale: before tile t rescales O at block j > 0, PV of its previous block (issue
+// index k - 2, with k = 2 j + t) must have completed.  The MMA thread issues S(k + 1) right after PV(k - 2), so
+// S(k + 1)'s commit covers it; in the one step with no S(k + 1) (tile 1 of the last block) the commit that
+// frees the K/V stage of block j - 1, also issued right after PV(k - 2), does.  Neither barrier can complete
+// a later phase before this warpgroup hands over P of block j, so the parity identifies the phase.
+template <int D>
+__device__ bool prev_pv_done(FwdBarriers* bars, int t, int j, int T, WaitCtl* wc) {
+    using C = FwdCfg<D>;
+    const int k1 = 2 * j + t + 1;
+    if (k1 < 2 * T) {
+        const int t1 = k1 & 1, j1 = k1 >> 1;
+        return warp_wait(&bars->s_full[t1][j1 & 1], (j1 >> 1) & 1, wc);
+    }
+    const int jp = j - 1;
+    return warp_wait(&bars->kv_empty[jp % C::kStages], (jp / C::kStages) & 1, wc);
 }
 
 template <int D, bool kStepNorm>
@@ -368,7 +393,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
         l_run = l_run * alpha + sum;
         if (j > 0 && __any_sync(0xffffffffu, rescale)) {
             // With three S buffers, PV of the previous block may still be accumulating into O.
-            if (C::kThreeS && !(ok = warp_wait(&bars->pv_done[t], (j - 1) & 1, wc))) break;
+            if (C::kThreeS && !(ok = prev_pv_done<D>(bars, t, j, T, wc))) break;
 #pragma unroll
             for (int q = 0; q < D / 32; ++q) {
                 uint32_t x[32];
@@ -537,7 +562,7 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     if (warp == kTmaWarp) {
         if (lane == 0) producer<D>(&tm_q, &tm_k, &tm_v, smem, bars, head, q0, kv0, T, starve);
     } else if (warp == kMmaWarp) {
-        if (lane == 0) mma_issuer<D>(smem, bars, tmem, T);
+        if (lane == 0) mma_issuer<D, kStepNorm>(smem, bars, tmem, T);
     } else {
         softmax_wg<D, kStepNorm>(bars, tmem, warp / 4, o, lse, head, q0, N, kv0, T, T_all, scale_log2,
                                  split ? reinterpret_cast<float*>(smem + C::kOffQ + 4096) : nullptr);

@@ -77,15 +77,17 @@ def test_bf16_peaky_rows_move_the_max_late(d):
     _check_full_bf16(fa, 1, 2, 1500, d, seed=400 + d, q_gain=4.0)
 
 
+@pytest.mark.parametrize("H,N", [(1, 1024), (160, 384)])
 @pytest.mark.parametrize("d", [64, 128])
-def test_bf16_increasing_scores_force_every_rescale(d):
-    """Keys ordered so every new block holds larger scores than all before it."""
+def test_bf16_increasing_scores_force_every_rescale(d, H, N):
+    """Keys ordered so every new block holds larger scores than all before it: every block rescales O,
+    the last one included.  One head of 1024 keys runs as split 2-CTA clusters only; 160 heads of 384
+    keys (a ragged last block) fill two full waves before the split tail."""
     fa = need_gpu()
-    N = 1024
     g = torch.Generator().manual_seed(7)
-    q = torch.ones(1, 1, N, d) / 4
-    k = (torch.linspace(0, 800, N)[:, None] * torch.ones(d) / d * 4).reshape(1, 1, N, d)
-    v = torch.randn(1, 1, N, d, generator=g)
+    q = torch.ones(1, H, N, d) / 4
+    k = (torch.linspace(0, 800, N)[:, None] * torch.ones(d) / d * 4).expand(1, H, N, d)
+    v = torch.randn(1, H, N, d, generator=g)
     inp = {n: t.to(torch.bfloat16).contiguous() for n, t in (("q", q), ("k", k), ("v", v))}
     scale = 1 / math.sqrt(d)
     o, lse = _run_bf16(fa, inp, scale)
