@@ -58,23 +58,32 @@ def _peaks():
 
 
 class ClockSampler:
-    """Samples SM clocks and throttle reasons with nvidia-smi while the timed region runs."""
+    """Samples SM clocks and throttle reasons with nvidia-smi every INTERVAL_MS while the timed region runs;
+    only samples whose own timestamp falls inside the region (mark_start .. mark_end) are reported."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, index: int):
         self.index = index
         self.proc = None
         self.lines = []
         self.thread = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.INTERVAL_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
             return
@@ -94,22 +103,40 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=5)
-        sm, smax, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+        return summarize_clock_lines(self.lines, self.t0, self.t1, self.INTERVAL_MS)
+
+
+def _smi_time(stamp: str):
+    """Seconds since the epoch of an nvidia-smi timestamp ('YYYY/MM/DD HH:MM:SS.mmm', local time)."""
+    try:
+        main, _, frac = stamp.strip().partition(".")
+        return time.mktime(time.strptime(main, "%Y/%m/%d %H:%M:%S")) + (float("0." + frac) if frac else 0.0)
+    except (ValueError, OverflowError):
+        return None
+
+
+def summarize_clock_lines(lines, t0, t1, interval_ms):
+    """Median SM clock, maximum clock and active throttle reasons of the samples taken between t0 and t1
+    (plus half a sampling interval either side); all samples if none carries a usable timestamp."""
+    names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+    rows = []
+    for line in lines:
+        parts = [p.strip() for p in line.split(",")]
+        if len(parts) < 10:
+            continue
+        try:
+            rows.append((_smi_time(parts[0]), float(parts[2]), float(parts[3]), parts[6:10]))
+        except ValueError:
+            continue
+    slack = interval_ms / 2000.0
+    timed = t0 is not None and t1 is not None and any(r[0] is not None for r in rows)
+    inside = [r for r in rows if r[0] is not None and t0 - slack <= r[0] <= t1 + slack] if timed else rows
+    sm = [r[1] for r in inside]
+    reasons = {n for r in inside for n, v in zip(names, r[3]) if v.lower() == "active"}
+    return {"sm_mhz": statistics.median(sm) if sm else None,
+            "sm_max_mhz": max(r[2] for r in inside) if inside else None,
+            "reasons": sorted(reasons), "samples": len(sm), "interval_ms": interval_ms,
+            "window": "timed region" if timed else "whole run (no timestamps)"}
 
 
 def _oracle_sample(w, heads: int, inp):
@@ -203,6 +230,7 @@ def run_ours(args, w):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     launches0 = fa.fa_kernel_launches()
+    clocks.mark_start()
     t_wall = time.perf_counter()
     for i in range(args.steps):
         flush.fill_(i & 0xff)                      # evict the previous step's data from L2 (untimed)
@@ -215,6 +243,7 @@ def run_ours(args, w):
     if world > 1:
         torch.distributed.barrier()
     wall = time.perf_counter() - t_wall
+    clocks.mark_end()
     launches = fa.fa_kernel_launches() - launches0          # counted by the library at each launch
     clk = clocks.stop()
     fa.fa_check_status(stream)
@@ -358,7 +387,7 @@ def _roofline(w, fwd_ms, bwd_ms, peaks):
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=fa_inputs.HEADLINE, choices=sorted(fa_inputs.WORKLOADS))
