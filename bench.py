@@ -387,7 +387,7 @@ def _roofline(w, fwd_ms, bwd_ms, peaks):
 def main():
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=fa_inputs.HEADLINE, choices=sorted(fa_inputs.WORKLOADS))
