@@ -42,7 +42,7 @@ BwdWorkspace bwd_workspace_layout(const Shape& s) {
     return w;
 }
 
-cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows) {
+static cudaError_t tmap_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
     static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
     if (!encode) {
         cudaDriverEntryPointQueryResult qres;
@@ -52,6 +52,29 @@ cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, 
         if (qres != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
         encode = (PFN_cuTensorMapEncodeTiled_v12000)fn;
     }
+    *out = encode;
+    return cudaSuccess;
+}
+
+cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int d, int N, int64_t heads, int box_cols,
+                             int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    cudaError_t e = tmap_encoder(&encode);
+    if (e != cudaSuccess) return e;
+    cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads};
+    cuuint64_t strides[2] = {(cuuint64_t)d * 4, (cuuint64_t)N * d * 4};
+    cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode;
+    cudaError_t e = tmap_encoder(&encode);
+    if (e != cudaSuccess) return e;
     cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
     cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};

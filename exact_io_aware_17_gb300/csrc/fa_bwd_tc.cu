@@ -73,7 +73,7 @@ struct BwdBarriers {
     uint64_t q_empty[2];           // dK of that step has read the Q tile
     uint64_t do_full[2];           // dO tile of a step in its slot
     uint64_t dv_done[2];           // dV of that step has read dO: the slot takes dS^T
-    uint64_t staged_a[2];          // the first half's dQ rows are in the slot
+    uint64_t staged_a[2][4];       // one 32-column stripe of the first half's dQ rows is in the slot
     uint64_t s_full;
     uint64_t dp_full;
     uint64_t p_ready[2];
@@ -110,6 +110,10 @@ struct BwdCfg {
     static constexpr uint32_t kOffQ = kOffV + kKBytes;
     static constexpr uint32_t kOffSlot = kOffQ + 2 * kQBytes;
     static constexpr uint32_t kOffStageB = kOffSlot + 2 * kSlotBytes;   // the second half's dQ rows
+    // The first half's rows are staged in the slot as stripes of 32 head-dimension columns ([HQ][32] fp32,
+    // one per warp), each added into the accumulator by a tensor reduce as soon as its warp has written it.
+    static constexpr int kStripes = D / 32;
+    static constexpr uint32_t kStripeBytes = HQ * 32 * 4;
     static constexpr uint32_t kRowBytes = BQ * 4;          // LSE2 or -D of one query block
     static constexpr uint32_t kOffRows = kOffStageB + kHalfDQBytes;    // [q stage][LSE2 | -D][BQ] floats
     static constexpr uint32_t kOffBar = kOffRows + 2 * 2 * kRowBytes;
@@ -126,6 +130,7 @@ struct BwdCfg {
     static_assert(kColDQ + 128 <= 512, "tensor memory columns");
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kQBytes <= kSlotBytes && kHalfDQBytes <= kSlotBytes, "slot contents");
+    static_assert(kStripes * kStripeBytes == kHalfDQBytes && kStripes <= 4, "stripes of the first half");
     static_assert(kSmemNeed <= 232448, "shared memory per CTA");
 };
 
@@ -137,7 +142,7 @@ __device__ __forceinline__ int qblock(int i, int rot, int Tq) {
 
 template <int D>
 __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, const CUtensorMap* tm_v,
-                             const CUtensorMap* tm_do, const float* lse2, const float* row_d,
+                             const CUtensorMap* tm_do, const CUtensorMap* tm_dq, const float* lse2, const float* row_d,
                              float* __restrict__ dq_acc, uint8_t* smem, BwdBarriers* bars, int head, int k0, int N,
                              int Tq, int Npad, int rot, int starve) {
     using C = BwdCfg<D>;
@@ -148,18 +153,17 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         tma_load_3d(smem + C::kOffK + c * C::kChunkK, tm_k, &bars->kv_full, c * 64, k0, head, pol_keep);
         tma_load_3d(smem + C::kOffV + c * C::kChunkK, tm_v, &bars->kv_full, c * 64, k0, head, pol_keep);
     }
-    // The first half's dQ rows of step j end up in slot j % 2.  This thread adds them into the
-    // accumulator and reloads the slot once the reduce has read it, so it owns the slot's whole cycle.
+    // The first half's dQ rows of step j end up in slot j % 2, one stripe per warp.  This thread adds each
+    // stripe into the accumulator as soon as it is there (rows past N are clipped by the tensor map) and
+    // reloads the slot once the reduces have read it, so it owns the slot's whole cycle.
     auto reduce_first_half = [&](int j) -> bool {
         const int t = j & 1;
-        if (!mbar_wait(&bars->staged_a[t], (j >> 1) & 1, wc)) return false;
         const int q0 = qblock(j, rot, Tq) * BQ;
-        const int rows = min(HQ, N - q0);
-        if (rows > 0) {
-            bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, smem + C::kOffSlot + t * C::kSlotBytes,
-                                (uint32_t)(rows * D * 4));
-            bulk_commit_group();
+        for (int w = 0; w < C::kStripes; ++w) {
+            if (!mbar_wait(&bars->staged_a[t][w], (j >> 1) & 1, wc)) return false;
+            tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kStripeBytes, 32 * w, q0, head);
         }
+        bulk_commit_group();
         return true;
     };
     int q_issued = 0, do_issued = 0;
@@ -399,9 +403,8 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(&bars->dq_empty);
-        // Stage rows [HQ][D] (fp32): the step's slot (dQ^T has read its dS^T) or the second half's buffer.
-        float* stage = reinterpret_cast<float*>(half == 0 ? smem + C::kOffSlot + s * C::kSlotBytes
-                                                          : smem + C::kOffStageB);
+        // Stage the rows (fp32): the first half into the step's slot (dQ^T has read its dS^T) as this warp's
+        // stripe [HQ][32], the second half into its own buffer as rows [HQ][D].
         // The second half's buffer is reused once the reduce of the previous step's rows has read it (it has
         // had a whole step); only the thread that issued that reduce can wait for it.
         if (half == 1 && i > 0) {
@@ -411,19 +414,32 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
             }
             if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
         }
-        if (dq_lane) {
+        if (half == 0) {
+            if (dq_lane) {
+                float* stripe =
+                    reinterpret_cast<float*>(smem + C::kOffSlot + s * C::kSlotBytes + quarter * C::kStripeBytes);
 #pragma unroll
-            for (int q = 0; q < HQ; ++q) stage[q * D + r] = __uint_as_float(x[q / 32][q % 32]);
+                for (int q = 0; q < HQ; ++q) stripe[q * 32 + lane] = __uint_as_float(x[q / 32][q % 32]);
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->staged_a[s][quarter]);
+            }
+        } else {
+            float* stage = reinterpret_cast<float*>(smem + C::kOffStageB);
+            if (dq_lane) {
+#pragma unroll
+                for (int q = 0; q < HQ; ++q) stage[q * D + r] = __uint_as_float(x[q / 32][q % 32]);
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(&bars->staged_b);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(half == 0 ? &bars->staged_a[s] : &bars->staged_b);
         // The TMA thread reduces the first half; the second half's leader reduces its own.  A wait that
         // gives up has set the abort flag, which stops the whole warp at its next wait.
         if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
             const int q0 = qblock(i, rot, Tq) * BQ + HQ;
             const int rows = min(HQ, N - q0);
             if (rows > 0) {
-                bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, stage, (uint32_t)(rows * D * 4));
+                bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, smem + C::kOffStageB,
+                                    (uint32_t)(rows * D * 4));
                 bulk_commit_group();
             }
         }
@@ -459,7 +475,7 @@ template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-              const float* __restrict__ lse2, const float* __restrict__ row_d, float* __restrict__ dq_acc,
+              const __grid_constant__ CUtensorMap tm_dq, const float* __restrict__ lse2, const float* __restrict__ row_d, float* __restrict__ dq_acc,
               __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int N, int Npad,
               int blocks_per_head, float scale, float scale_log2, long long wait_budget, int starve) {
     using C = BwdCfg<D>;
@@ -488,7 +504,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&bars->q_empty[t], 1);
             mbar_init(&bars->do_full[t], 1);
             mbar_init(&bars->dv_done[t], 1);
-            mbar_init(&bars->staged_a[t], 128);
+            for (int w = 0; w < 4; ++w) mbar_init(&bars->staged_a[t][w], 32);
             mbar_init(&bars->p_ready[t], 128);
             mbar_init(&bars->ds_ready[t], 128);
         }
@@ -513,6 +529,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tma_prefetch_desc(&tm_k);
         tma_prefetch_desc(&tm_v);
         tma_prefetch_desc(&tm_do);
+        tma_prefetch_desc(&tm_dq);
     }
     if (warp == kMmaWarp) {
         tmem_alloc(&bars->tmem_base, C::kTmemCols);
@@ -525,7 +542,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
 
     if (warp == kTmaWarp) {
         if (lane == 0)
-            bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, lse2, row_d, dq_acc, smem, bars, head, k0, N, Tq, Npad, rot,
+            bwd_producer<D>(&tm_q, &tm_k, &tm_v, &tm_do, &tm_dq, lse2, row_d, dq_acc, smem, bars, head, k0, N, Tq, Npad, rot,
                             starve);
     } else if (warp == kMmaWarp) {
         if (lane == 0) bwd_mma<D>(smem, bars, tmem, Tq);
@@ -629,18 +646,19 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     if (e != cudaSuccess) return e;
     count_launches(1);
 
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if ((e = make_tmap_bf16_3d(&tq, q, s.d, s.N, s.heads(), BQ)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tdo, dout, s.d, s.N, s.heads(), BQ)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tk, k, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
+    if ((e = make_tmap_f32_3d(&tdq, dq_acc, s.d, s.N, s.heads(), 32, HQ)) != cudaSuccess) return e;
     e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int bph = (s.N + BK - 1) / BK;
     if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
     const unsigned grid = (unsigned)(bph * s.heads());
     const WaitPolicy wp = wait_policy();
-    bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, lse2, row_d, dq_acc,
+    bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse2, row_d, dq_acc,
                                                             (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, s.N, Npad, bph, scale,
                                                             scale * 1.4426950408889634f, wp.budget_cycles, wp.starve);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;

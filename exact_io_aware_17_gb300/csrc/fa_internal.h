@@ -48,6 +48,10 @@ int device_sm_count();
 // Encodes a TMA descriptor for a bf16 [heads, N, d] array (d innermost) with boxes of 64 columns x
 // `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows);
+// fp32 [heads][N][d] viewed as (d, N, heads), unswizzled boxes of box_cols x box_rows (box_cols * 4 bytes a
+// multiple of 16): the dQ accumulator as the target of tensor reduce-adds.
+cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int d, int N, int64_t heads, int box_cols,
+                             int box_rows);
 
 // Launchers (return cudaGetLastError() of their launches).
 cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& s,

@@ -153,6 +153,14 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssr
                  "r"(smem_u32(ssrc)), "r"(bytes)
                  : "memory");
 }
+// Tensor reduce-add: the shared-memory box at `ssrc` (the tensor map's box, element type and layout) is added
+// into the 3-D tensor at (x, y, z); rows past the tensor's extent are clipped.  Completion is tracked by the
+// issuing thread's bulk groups.  x times the element size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_reduce_add_3d(const CUtensorMap* map, const void* ssrc, int x, int y, int z) {
+    asm volatile("cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::
+                     "l"(map), "r"(smem_u32(ssrc)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void bulk_wait_group_read() {
