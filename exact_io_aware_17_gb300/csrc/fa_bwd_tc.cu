@@ -21,7 +21,9 @@
 //                         dK_j += dS^T Q_i              dS^T as bf16 from tensor memory
 //                         dQ_i^T = K_j^T dS^T           dS^T as bf16 from shared memory, into the
 //                                                       columns of dP^T (free once dK used dS^T)
-//                     and adds dQ_i into the fp32 accumulator with bulk reduce-add copies.
+//                     and adds dQ_i into the fp32 accumulator with bulk reduce-add copies (the first
+//                     half's rows as one tensor reduce per 32-column stripe, the second half's as one
+//                     linear reduce).
 //   bwd_dq_convert    dQ = bf16(scale * accumulator).
 //
 // Every product is 128 x 128 x 128 (M = 128 keys or head dimensions, N = 128 queries or head
@@ -39,8 +41,9 @@
 // from its own leader thread.
 //
 // Shared memory (d = 128: 226 KB): K and V resident, two Q stages, and two slots that each hold a step's dO
-// tile, then its dS^T (once dV has read dO), then the first half's fp32 dQ rows (once dQ^T has read dS^T);
-// the TMA thread adds those rows into the accumulator and loads the dO tile of step i + 2 there.  The
+// tile, then its dS^T (once dV has read dO), then the first half's fp32 dQ rows (once dQ^T has read dS^T),
+// one [64][32] stripe per warp; the TMA thread adds each stripe into the accumulator as soon as its warp
+// has written it and, once the reduces have read the slot, loads the dO tile of step i + 2 there.  The
 // second half's dQ rows have a buffer of their own.  The kernel has no static shared memory, so its
 // dynamic region starts aligned and needs no slack.
 //
