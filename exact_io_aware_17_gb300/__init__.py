@@ -75,9 +75,9 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream):
+def _stream(stream, device=None):
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
 
 
@@ -91,22 +91,26 @@ def _default_scale(d, scale):
     return 1.0 / math.sqrt(d) if scale is None else float(scale)
 
 
-def _check_tensor(name, t, shape, dtype):
+def _check_tensor(name, t, shape, dtype, device=None):
     if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
         raise ValueError(f"{name}: expected a contiguous CUDA {dtype} tensor of shape {tuple(shape)}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name}: on {t.device}, expected {device} (every tensor of a call on one GPU)")
 
 
 def fa_fwd(q, k, v, scale=None, o=None, lse=None, stream=None, _entry="fa_fwd"):
     """bf16 forward: returns (o bf16 [B,H,N,d], lse fp32 [B,H,N])."""
     B, H, N, d = _shape(q)
+    dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_tensor(name, t, (B, H, N, d), torch.bfloat16)
+        _check_tensor(name, t, (B, H, N, d), torch.bfloat16, dev)
     o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check_tensor("o", o, (B, H, N, d), torch.bfloat16)
-    _check_tensor("lse", lse, (B, H, N), torch.float32)
-    _check(getattr(load_library(), _entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                           _default_scale(d, scale), _stream(stream)))
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev) if lse is None else lse
+    _check_tensor("o", o, (B, H, N, d), torch.bfloat16, dev)
+    _check_tensor("lse", lse, (B, H, N), torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check(getattr(load_library(), _entry)(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                               _default_scale(d, scale), _stream(stream, dev)))
     return o, lse
 
 
@@ -118,14 +122,16 @@ def fa_fwd_stepnorm(q, k, v, scale=None, o=None, lse=None, stream=None):
 def fa_fwd_f32(q, k, v, scale=None, o=None, lse=None, stream=None):
     """fp32 forward: returns (o fp32 [B,H,N,d], lse fp32 [B,H,N])."""
     B, H, N, d = _shape(q)
+    dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_tensor(name, t, (B, H, N, d), torch.float32)
+        _check_tensor(name, t, (B, H, N, d), torch.float32, dev)
     o = torch.empty_like(q) if o is None else o
-    lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device) if lse is None else lse
-    _check_tensor("o", o, (B, H, N, d), torch.float32)
-    _check_tensor("lse", lse, (B, H, N), torch.float32)
-    _check(load_library().fa_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
-                                     _default_scale(d, scale), _stream(stream)))
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev) if lse is None else lse
+    _check_tensor("o", o, (B, H, N, d), torch.float32, dev)
+    _check_tensor("lse", lse, (B, H, N), torch.float32, dev)
+    with torch.cuda.device(dev):
+        _check(load_library().fa_fwd_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), B, H, N, d,
+                                         _default_scale(d, scale), _stream(stream, dev)))
     return o, lse
 
 
@@ -137,17 +143,32 @@ def fa_bwd(q, k, v, o, do, lse, scale=None, dq=None, dk=None, dv=None, workspace
     """bf16 backward: returns (dq, dk, dv), bf16 [B,H,N,d].  ``workspace`` is a uint8 CUDA tensor of at
     least fa_bwd_workspace_size(B,H,N,d) bytes; one is allocated by torch if not given."""
     B, H, N, d = _shape(q)
+    dev = q.device
+    dq, dk, dv = _bwd_outputs(q, k, v, o, do, lse, dq, dk, dv)
+    if workspace is None:
+        workspace = torch.empty(fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
+    if not workspace.is_cuda or workspace.device != dev or not workspace.is_contiguous():
+        raise ValueError(f"workspace: expected a contiguous tensor on {dev}")
+    with torch.cuda.device(dev):
+        _check(load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
+                                     _ptr(dv), B, H, N, d, _default_scale(d, scale), _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _stream(stream, dev)))
+    return dq, dk, dv
+
+
+def _bwd_outputs(q, k, v, o, do, lse, dq, dk, dv):
+    """Checks the backward's inputs and caller-given outputs (dtype, shape, contiguity, one device) and
+    allocates the outputs not given."""
+    B, H, N, d = _shape(q)
+    dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
-        _check_tensor(name, t, (B, H, N, d), torch.bfloat16)
-    _check_tensor("lse", lse, (B, H, N), torch.float32)
+        _check_tensor(name, t, (B, H, N, d), torch.bfloat16, dev)
+    _check_tensor("lse", lse, (B, H, N), torch.float32, dev)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    if workspace is None:
-        workspace = torch.empty(fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=q.device)
-    _check(load_library().fa_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq), _ptr(dk),
-                                 _ptr(dv), B, H, N, d, _default_scale(d, scale), _ptr(workspace),
-                                 workspace.numel() * workspace.element_size(), _stream(stream)))
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_tensor(name, t, (B, H, N, d), torch.bfloat16, dev)
     return dq, dk, dv
 
 
@@ -157,14 +178,12 @@ def fa_bwd_noalloc(q, k, v, o, do, lse, scale=None, dq=None, dk=None, dv=None, s
     the call allocate nothing at all; shapes needing more than NOALLOC_MAX_SCRATCH_BYTES of scratch
     raise FAError (FA_ERR_INVALID_ARG)."""
     B, H, N, d = _shape(q)
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("do", do)):
-        _check_tensor(name, t, (B, H, N, d), torch.bfloat16)
-    _check_tensor("lse", lse, (B, H, N), torch.float32)
-    dq = torch.empty_like(q) if dq is None else dq
-    dk = torch.empty_like(k) if dk is None else dk
-    dv = torch.empty_like(v) if dv is None else dv
-    _check(load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
-                                         _ptr(dk), _ptr(dv), B, H, N, d, _default_scale(d, scale), _stream(stream)))
+    dev = q.device
+    dq, dk, dv = _bwd_outputs(q, k, v, o, do, lse, dq, dk, dv)
+    with torch.cuda.device(dev):
+        _check(load_library().fa_bwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                             _ptr(dk), _ptr(dv), B, H, N, d, _default_scale(d, scale),
+                                             _stream(stream, dev)))
     return dq, dk, dv
 
 

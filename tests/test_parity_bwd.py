@@ -207,3 +207,27 @@ def test_bwd_dk_dv_bitwise_repeatable_dq_within_rounding(H, N, d):
     dq2, dk2, dv2 = r2
     assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
     assert (dq1.float() - dq2.float()).abs().max().item() <= 1e-2 * dq1.float().abs().max().item()
+
+
+def test_bwd_rejects_bad_caller_outputs_and_workspace():
+    """Caller-given dq/dk/dv and workspace are checked before the library is called (a wrong dtype or shape
+    would otherwise let the kernels write past the end of the buffer)."""
+    fa = need_gpu()
+    B, H, N, d = 1, 2, 256, 64
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed=79, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fa_fwd(q, k, v)
+    launches = fa.fa_kernel_launches()
+    bad = [dict(dq=torch.empty(B, H, N, d, dtype=torch.float32, device="cuda")),
+           dict(dk=torch.empty(B, H, N - 1, d, dtype=torch.bfloat16, device="cuda")),
+           dict(dv=torch.empty(B, H, N, d, dtype=torch.bfloat16, device="cuda").transpose(2, 3).contiguous()
+                .transpose(2, 3)),
+           dict(workspace=torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8))]
+    for kw in bad:
+        with pytest.raises(ValueError):
+            fa.fa_bwd(q, k, v, o, do, lse, **kw)
+    for kw in bad[:3]:
+        with pytest.raises(ValueError):
+            fa.fa_bwd_noalloc(q, k, v, o, do, lse, **kw)
+    torch.cuda.synchronize()
+    assert fa.fa_kernel_launches() == launches    # nothing was launched
