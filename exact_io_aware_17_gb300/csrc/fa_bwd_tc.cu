@@ -74,7 +74,7 @@ struct BwdBarriers {
     uint64_t kv_full;
     uint64_t q_full[2];            // Q tile + LSE2 and -D rows of a step
     uint64_t q_empty[2];           // dK of that step has read the Q tile
-    uint64_t do_full[2];           // dO tile of a step in its slot
+    uint64_t do_full[2][2];        // [slot][64-column chunk]: that chunk of a step's dO tile is in its slot
     uint64_t dv_done[2];           // dV of that step has read dO: the slot takes dS^T
     uint64_t staged_a[2][4];       // one 32-column stripe of the first half's dQ rows is in the slot
     uint64_t s_full;
@@ -159,14 +159,16 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
     // The first half's dQ rows of step j end up in slot j % 2, one stripe per warp.  This thread adds each
     // stripe into the accumulator as soon as it is there (rows past N are clipped by the tensor map) and
     // reloads the slot once the reduces have read it, so it owns the slot's whole cycle.
+    // One bulk group per 64-column chunk of the dO tile that reloads the slot (the stripes under chunk c),
+    // so that chunk c can load as soon as its group has been read.
     auto reduce_first_half = [&](int j) -> bool {
         const int t = j & 1;
         const int q0 = qblock(j, rot, Tq) * BQ;
         for (int w = 0; w < C::kStripes; ++w) {
             if (!mbar_wait(&bars->staged_a[t][w], (j >> 1) & 1, wc)) return false;
             tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kStripeBytes, 32 * w, q0, head);
+            if ((w + 1) % (C::kStripes / C::kChunks) == 0) bulk_commit_group();
         }
-        bulk_commit_group();
         return true;
     };
     int q_issued = 0, do_issued = 0;
@@ -190,14 +192,17 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
             q_issued = i + 1;
         }
 
-        if (i >= 2) {
-            if (!(ok = reduce_first_half(i - 2))) break;
-            bulk_wait_group_read<0>();
-        }
-        mbar_expect_tx(&bars->do_full[s], C::kQBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-            tma_load_3d(smem + C::kOffSlot + s * C::kSlotBytes + c * C::kChunkQ, tm_do, &bars->do_full[s], c * 64,
+        if (i >= 2 && !(ok = reduce_first_half(i - 2))) break;
+        for (int c = 0; c < C::kChunks; ++c) {
+            // Chunk c overwrites the stripes of reduce group c (the groups are read in order).
+            if (i >= 2) {
+                if (C::kChunks == 2 && c == 0) bulk_wait_group_read<1>();
+                else bulk_wait_group_read<0>();
+            }
+            mbar_expect_tx(&bars->do_full[s][c], C::kChunkQ);
+            tma_load_3d(smem + C::kOffSlot + s * C::kSlotBytes + c * C::kChunkQ, tm_do, &bars->do_full[s][c], c * 64,
                         qb * BQ, head, pol_keep);
+        }
         do_issued = i + 1;
     }
     for (int j = (Tq > 2 ? Tq - 2 : 0); ok && j < Tq; ++j) ok = reduce_first_half(j);
@@ -206,7 +211,7 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
     drain_wait(&bars->kv_full, 0, wc);
     for (int i = (q_issued > 2 ? q_issued - 2 : 0); i < q_issued; ++i) drain_wait(&bars->q_full[i & 1], (i >> 1) & 1, wc);
     for (int i = (do_issued > 2 ? do_issued - 2 : 0); i < do_issued; ++i)
-        drain_wait(&bars->do_full[i & 1], (i >> 1) & 1, wc);
+        for (int c = 0; c < C::kChunks; ++c) drain_wait(&bars->do_full[i & 1][c], (i >> 1) & 1, wc);
 }
 
 // MMA order of step i: dV(i), S^T(i+1), dK(i), dQ^T(i), dP^T(i+1).  S^T of the next step goes right
@@ -255,15 +260,34 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
             mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(b0, kk * 16 * 128), idQ, kk > 0);
     };
 
+    // dP^T = V dO^T for the dO tile in `slot`, one 64-column chunk of the head dimension (four k-steps) at
+    // a time: chunk 0 has been waited for by the caller; each further chunk is waited for here, so the
+    // first k-steps run while the rest of the tile is still landing.
+    auto dp_by_chunks = [&](int slot, uint32_t ph) -> bool {
+        const uint64_t b0 = sdesc_advance(kDO, slot * C::kSlotBytes);
+        const uint32_t d = tmem + C::kColDP;
+#pragma unroll
+        for (int c = 0; c < C::kChunks; ++c) {
+            if (c > 0) {
+                if (!mbar_wait_poll(&bars->do_full[slot][c], ph, wc)) return false;
+                tc_fence_after();
+            }
+#pragma unroll
+            for (int kk = 4 * c; kk < 4 * c + 4; ++kk)
+                mma_ss(d, sdesc_advance(kV, (kk / 4) * C::kChunkK + (kk % 4) * 32),
+                       sdesc_advance(b0, (kk / 4) * C::kChunkQ + (kk % 4) * 32), idS, kk > 0);
+        }
+        return true;
+    };
+
     bool ok = mbar_wait_poll(&bars->kv_full, 0, wc) && mbar_wait_poll(&bars->q_full[0], 0, wc);
     if (ok) {
         tc_fence_after();
         qk_like(kK, kQ, C::kColS);
         mma_commit(&bars->s_full);
-        if ((ok = mbar_wait_poll(&bars->do_full[0], 0, wc))) {
+        if ((ok = mbar_wait_poll(&bars->do_full[0][0], 0, wc))) {
             tc_fence_after();
-            qk_like(kV, kDO, C::kColDP);
-            mma_commit(&bars->dp_full);
+            if ((ok = dp_by_chunks(0, 0))) mma_commit(&bars->dp_full);
         }
     }
     for (int i = 0; ok && i < Tq; ++i) {
@@ -294,11 +318,11 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         dq(sdesc_advance(mDS, s * C::kSlotBytes));
         mma_commit(&bars->dq_full);
         if (i + 1 < Tq) {
-            if (!(ok = mbar_wait_poll(&bars->do_full[s1], ((i + 1) >> 1) & 1, wc))) break;
+            if (!(ok = mbar_wait_poll(&bars->do_full[s1][0], ((i + 1) >> 1) & 1, wc))) break;
             // At d = 128 the columns of dP^T hold dQ^T of step i until it has been moved out.
             if (!C::kOwnDQ && !(ok = mbar_wait_poll(&bars->dq_empty, i & 1, wc))) break;
             tc_fence_after();
-            qk_like(kV, sdesc_advance(kDO, s1 * C::kSlotBytes), C::kColDP);
+            if (!(ok = dp_by_chunks(s1, ((i + 1) >> 1) & 1))) break;
             mma_commit(&bars->dp_full);
         }
     }
@@ -505,7 +529,8 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->q_full[t], 1);
             mbar_init(&bars->q_empty[t], 1);
-            mbar_init(&bars->do_full[t], 1);
+            mbar_init(&bars->do_full[t][0], 1);
+            mbar_init(&bars->do_full[t][1], 1);
             mbar_init(&bars->dv_done[t], 1);
             for (int w = 0; w < 4; ++w) mbar_init(&bars->staged_a[t][w], 32);
             mbar_init(&bars->p_ready[t], 128);
