@@ -354,7 +354,7 @@ def _e2e(fa, w, inp_cpu, dev, steps):
 # DRAM bytes per launch of the dominant kernel at the bench workload, from one ncu capture of the
 # kernel as it is built now (dram__bytes_read.sum + dram__bytes_write.sum).  Set to None whenever the
 # kernel changes until it is measured again.
-TRAFFIC_BYTES = {("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): None}
+TRAFFIC_BYTES = {("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): 202915584 + 83937024}
 
 
 # Measured throughput of the exponential unit (ex2.approx.f32, whole GPU), the second ceiling of the

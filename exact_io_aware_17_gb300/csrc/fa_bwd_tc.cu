@@ -43,7 +43,8 @@
 // Shared memory (d = 128: 226 KB): K and V resident, two Q stages, and two slots that each hold a step's dO
 // tile, then its dS^T (once dV has read dO), then the first half's fp32 dQ rows (once dQ^T has read dS^T),
 // one [64][32] stripe per warp; the TMA thread adds each stripe into the accumulator as soon as its warp
-// has written it and, once the reduces have read the slot, loads the dO tile of step i + 2 there.  The
+// has written it and loads the dO tile of step i + 2 there by 64-column chunks, each once the stripes
+// under it have been read; the MMA thread starts dP^T(i+2) on the first chunk.  The
 // second half's dQ rows have a buffer of their own.  The kernel has no static shared memory, so its
 // dynamic region starts aligned and needs no slack.
 //
