@@ -54,6 +54,7 @@ typedef enum {
  *   lse     : float [B,H,N]               (output, natural-log log-sum-exp of each scaled score row)
  *   d       : 64 or 128 (FA_ERR_UNSUPPORTED otherwise).  N may be any value >= 1 (ragged tails are masked).
  *   Product B*H must fit in 2^31 - 1; N*d in 2^31 - 1.
+ *   Repeatability: the same inputs give the same bits on every call (no atomics; fixed block order).
  */
 fa_status fa_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
                  int B, int H, int N, int d, float scale, void* stream);
@@ -99,6 +100,8 @@ size_t fa_bwd_workspace_size(int B, int H, int N, int d);
  *   d          : 64 or 128.
  * P is recomputed tile by tile from q, k and lse (it is never stored); dV = P^T dO, dP = dO V^T,
  * dS = P o (dP - D), dK = scale dS^T Q, dQ = scale dS K with D_i = dO_i . O_i.
+ * Repeatability: dk and dv are the same bits on every call with the same inputs; dq sums per-key-block
+ * contributions whose order varies between calls, so its last bits may differ (within rounding).
  */
 fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                  const float* lse, void* dq, void* dk, void* dv,
