@@ -32,7 +32,9 @@
 //     m = max(m0, m1),  l = 2^(m0-m) l0 + 2^(m1-m) l1,  O = (2^(m0-m) O0 + 2^(m1-m) O1) / l,
 // the same exp-sum factorisation as the online rescale.  The last wave then takes half as long.
 //
-// TMEM columns: S0/P0 [0,128), S1/P1 [128,256), O0 [256,256+D), O1 [256+D,256+2D).
+// TMEM columns at d = 128: S0/P0 [0,128), S1/P1 [128,256), O0 [256,384), O1 [384,512).  At d = 64 S rotates
+// through three buffers [0,128), [128,256), [256,384) (S of the next tile is formed while the softmax works
+// on the current one), O0 [384,448), O1 [448,512); K and V share one barrier per ring stage.
 
 #include <cuda_bf16.h>
 #include <math.h>
