@@ -186,9 +186,15 @@ def run_reference(args, w):
 METRIC = "attention TFLOP/s fwd and fwd+bwd vs BF16 tensor peak (N=8192, d=128, 1xGB300)"
 
 
-def _config(w, world):
+def _config(w, world, strong=False):
+    if world == 1:
+        par = "single-gpu"
+    elif strong:
+        par = f"heads{world}: the workload's B*H heads split into contiguous ranges, one per rank, no collective"
+    else:
+        par = f"batches{world}: each rank its own batch of the workload's shape (seed + rank), no collective"
     return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "dtype": w.dtype,
-            "step": "fa_fwd + fa_bwd", "parallelism": f"replicas{world}" if world > 1 else "single-gpu",
+            "step": "fa_fwd + fa_bwd", "parallelism": par,
             "l2": f"flushed between timed steps ({L2_FLUSH_BYTES >> 20} MiB write, untimed)"}
 
 
@@ -203,9 +209,20 @@ def run_ours(args, w):
     dev = torch.device("cuda", local)
     fa.load_library()
 
-    inp_cpu = fa_inputs.workload_inputs(w, with_grad=True)
+    strong = args.strong and world > 1
+    if strong:
+        # Strong scaling: the one workload, its heads split across the ranks (each rank holds only its own).
+        from exact_io_aware_17_gb300 import shard
+        full = fa_inputs.workload_inputs(w, with_grad=True)
+        inp_cpu = {n: shard.local_heads(t, rank, world).contiguous() for n, t in full.items()}
+        heads_here = inp_cpu["q"].shape[1]
+        if heads_here == 0:
+            raise SystemExit(f"--strong: rank {rank} of {world} would get no head of {w.name}")
+    else:
+        # One GPU, or weak scaling: every rank runs the whole workload's shape on its own batch.
+        inp_cpu = fa_inputs.make_inputs(w.B, w.H, w.N, w.d, w.dtype, w.seed + rank, w.q_gain, with_grad=True)
     q, k, v, do = (inp_cpu[n].to(dev) for n in ("q", "k", "v", "do"))
-    B, H, N, d = w.B, w.H, w.N, w.d
+    B, H, N, d = (int(x) for x in q.shape)
     o = torch.empty_like(q)
     lse = torch.empty(B, H, N, dtype=torch.float32, device=dev)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
@@ -252,23 +269,26 @@ def run_ours(args, w):
     bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
     step_ms = sum(fwd_ms) / args.steps + sum(bwd_ms) / args.steps
     step_ms = max_over_ranks(step_ms, dev)
-    total_flops = (w.fwd_flops() + w.bwd_flops()) * world
+    # Work of this rank's heads, and of the whole job (all ranks) per step.
+    lw = fa_inputs.Workload(w.name, w.dtype, B, H, N, d, w.seed)
+    total_flops = (w.fwd_flops() + w.bwd_flops()) * (1 if strong else world)
     value = total_flops / (step_ms * 1e-3) / 1e12
     fwd_avg = sum(fwd_ms) / args.steps
     bwd_avg = sum(bwd_ms) / args.steps
-    fwd_tflops = w.fwd_flops() / (fwd_avg * 1e-3) / 1e12
-    bwd_tflops = w.bwd_flops() / (bwd_avg * 1e-3) / 1e12
+    fwd_tflops = lw.fwd_flops() / (fwd_avg * 1e-3) / 1e12
+    bwd_tflops = lw.bwd_flops() / (bwd_avg * 1e-3) / 1e12
     peaks = _peaks()
     peak = peaks["bf16_tflops"]
 
-    e2e_ms, h2d, d2h = _e2e(fa, w, inp_cpu, dev, args.steps)
+    e2e_ms, h2d, d2h = _e2e(fa, lw, inp_cpu, dev, args.steps)
     e2e_ms = max_over_ranks(e2e_ms, dev)
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-        "warmup": max(args.warmup, 3), "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak",
+        "warmup": max(args.warmup, 3), "ms_per_step": step_ms, "higher_is_better": True,
+        "scaling": "strong" if strong else "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded iid N(0,1), bf16)",
-        "config": _config(w, world),
+        "config": _config(w, world, strong),
         "fwd": {"ms": fwd_avg, "tflops": fwd_tflops, "frac_of_peak": fwd_tflops / peak},
         "bwd": {"ms": bwd_avg, "tflops": bwd_tflops, "frac_of_peak": bwd_tflops / peak},
         "fwd_bwd_frac_of_peak": value / world / peak,
@@ -276,15 +296,15 @@ def run_ours(args, w):
         "clocks": clk,
         "gpu_launches": launches,
         "gpu_launches_counted_by": "libfa.so's own launch counter (fa_kernel_launches) across the timed loop",
-        "e2e": {"value": (w.fwd_flops() + w.bwd_flops()) * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q,k,v,dO copied in and o,lse,dq,dk,dv copied out every step, through the "
                        "public API; copies run on two copy streams, double-buffered so that step i's "
                        "transfers overlap steps i-1 and i+1's compute"},
     }
-    line["roofline"] = _roofline(w, fwd_avg, bwd_avg, peaks)
-    line["exp_pipe"] = _exp_pipe(w, fwd_avg, bwd_avg)
-    if rank == 0 and not args.no_cpu_baseline:
+    line["roofline"] = _roofline(lw if strong else w, fwd_avg, bwd_avg, peaks)
+    line["exp_pipe"] = _exp_pipe(lw, fwd_avg, bwd_avg)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, t = _oracle_sample(w, args.oracle_heads, inp_cpu)
         meta = _cpu_meta(args.oracle_heads, w)
         meta.update({"value": f / t / 1e12, "unit": "TFLOP/s", "seconds": t})
@@ -351,10 +371,37 @@ def _e2e(fa, w, inp_cpu, dev, steps):
     return start.elapsed_time(end) / steps, 4 * elt, 4 * elt + B * H * N * 4
 
 
-# DRAM bytes per launch of the dominant kernel at the bench workload, from one ncu capture of the
-# kernel as it is built now (dram__bytes_read.sum + dram__bytes_write.sum).  Set to None whenever the
-# kernel changes until it is measured again.
-TRAFFIC_BYTES = {("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): 202915584 + 83937024}
+# DRAM bytes per launch of the dominant kernel at the bench workload, from one ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), with the profile summary that records it and the
+# SHA-256 of the kernel's source files when it was taken.  If the sources differ now, the figure is
+# stale: the JSON line then reports traffic null and says so.
+TRAFFIC = {
+    ("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): {
+        "bytes": 202915584 + 83937024,
+        "profile": "profiles/dram_per_launch_bench_B1-H16-N8192-d128.md",
+        "kernel": "bwd_tc_kernel<128>",
+        "sources": ("exact_io_aware_17_gb300/csrc/fa_bwd_tc.cu", "exact_io_aware_17_gb300/csrc/fa_ptx.cuh"),
+        "sha256": "02ca527aed86d07f37ec5cd5667d5a69f4cbf45bbe319c147f3efe44b7eec991",
+    },
+}
+
+
+def _sources_digest(paths):
+    import hashlib
+    h = hashlib.sha256()
+    for rel in paths:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def _traffic(name, w):
+    t = TRAFFIC.get((name, w.name))
+    if t is None:
+        return None, "no capture for this kernel and workload"
+    if t["sha256"] != _sources_digest(t["sources"]):
+        return None, f"stale: {t['kernel']} sources changed since the capture in {t['profile']}"
+    return t["bytes"], f"ncu capture of {t['kernel']}, {t['profile']}"
 
 
 # Measured throughput of the exponential unit (ex2.approx.f32, whole GPU), the second ceiling of the
@@ -379,9 +426,92 @@ def _roofline(w, fwd_ms, bwd_ms, peaks):
         name, flops, ms = "forward", w.fwd_flops(), fwd_ms
     achieved = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
+    traffic, source = _traffic(name, w)
     return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
             "frac": achieved / peak, "peak_source": f"{peaks['source']} burst bf16 (cuBLAS)",
-            "traffic": TRAFFIC_BYTES.get((name, w.name)), "traffic_unit": "bytes per launch (bwd_tc_kernel, ncu)"}
+            "traffic": traffic, "traffic_unit": "DRAM bytes per launch of the main kernel", "traffic_source": source}
+
+
+def _time_call(fn, flush, iters):
+    """Median CUDA-event time (ms) of fn() over `iters` calls, L2 flushed before each, after 3 warm-ups."""
+    for _ in range(3):
+        fn()
+    ts = []
+    for i in range(iters):
+        flush.fill_(i & 0xFF)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def run_sweep(args):
+    """Throughput over shapes, one JSON line per shape (not the bench contract line).
+
+    Grid mode: B=1, d in --d, N in --N, H = --rows // N (so every shape has the same B*H*N rows), seeded
+    N(0,1) bf16 inputs.  Workload mode (--workloads): the named workloads' own shapes and inputs; --bwd times
+    the backward of forward-only workloads too (their upstream gradient dO is drawn after Q, K, V by the
+    same seeded generator, so Q, K, V are the workload's own).  Median of --iters CUDA-event timings per call,
+    L2 flushed between calls; fractions of the measured bf16 burst peak."""
+    import exact_io_aware_17_gb300 as fa
+    peaks = _peaks()
+    peak = peaks["bf16_tflops"]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    if args.workloads:
+        shapes = [(fa_inputs.WORKLOADS[n], fa_inputs.WORKLOADS[n].backward or args.bwd) for n in args.workloads]
+    else:
+        shapes = []
+        for d in args.d:
+            for N in args.N:
+                H = max(1, args.rows // N)
+                shapes.append((fa_inputs.Workload(f"B1-H{H}-N{N}-d{d}", "bf16", 1, H, N, d, seed=N + d), True))
+    for w, with_bwd in shapes:
+        if w.dtype != "bf16":
+            continue
+        inp = fa_inputs.workload_inputs(w, with_grad=with_bwd)
+        t = {n: x.cuda() for n, x in inp.items()}
+        o, lse = fa.fa_fwd(t["q"], t["k"], t["v"], w.scale)
+        tf = _time_call(lambda: fa.fa_fwd(t["q"], t["k"], t["v"], w.scale, o, lse), flush, args.iters)
+        line = {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "fwd_ms": tf,
+                "fwd_tflops": w.fwd_flops() / tf / 1e9, "fwd_frac": w.fwd_flops() / tf / 1e9 / peak}
+        if with_bwd:
+            dq, dk, dv = (torch.empty_like(t["q"]) for _ in range(3))
+            ws = torch.empty(fa.fa_bwd_workspace_size(w.B, w.H, w.N, w.d), dtype=torch.uint8, device="cuda")
+            tb = _time_call(lambda: fa.fa_bwd(t["q"], t["k"], t["v"], o, t["do"], lse, w.scale, dq, dk, dv, ws),
+                            flush, args.iters)
+            line.update(bwd_ms=tb, bwd_tflops=w.bwd_flops() / tb / 1e9, bwd_frac=w.bwd_flops() / tb / 1e9 / peak,
+                        fwdbwd_tflops=(w.fwd_flops() + w.bwd_flops()) / (tf + tb) / 1e9,
+                        fwdbwd_frac=(w.fwd_flops() + w.bwd_flops()) / (tf + tb) / 1e9 / peak)
+        if args.stepnorm:
+            tsn = _time_call(lambda: fa.fa_fwd_stepnorm(t["q"], t["k"], t["v"], w.scale, o, lse), flush, args.iters)
+            line.update(stepnorm_fwd_ms=tsn, stepnorm_fwd_tflops=w.fwd_flops() / tsn / 1e9, stepnorm_slowdown=tsn / tf)
+        fa.fa_check_status()
+        line.update(peak_tflops=peak, peak_source=peaks["source"])
+        print(json.dumps(line), flush=True)
+        del t, o, lse
+        torch.cuda.empty_cache()
+    return 0
+
+
+def run_case(args):
+    """A fixed, small command for profilers: --iters forward (and with --bwd backward) calls on one seeded
+    bf16 shape B H N d, then a status check.  Prints "ok"."""
+    import exact_io_aware_17_gb300 as fa
+    B, H, N, d = args.case
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed=5, with_grad=args.bwd)
+    t = {n: x.cuda() for n, x in inp.items()}
+    scale = 1 / math.sqrt(d)
+    for _ in range(args.iters):
+        o, lse = fa.fa_fwd(t["q"], t["k"], t["v"], scale)
+        if args.bwd:
+            fa.fa_bwd(t["q"], t["k"], t["v"], o, t["do"], lse, scale)
+    torch.cuda.synchronize()
+    fa.fa_check_status()
+    print("ok")
+    return 0
 
 
 def main():
@@ -396,7 +526,25 @@ def main():
     ap.add_argument("--oracle-heads-per-step", type=int, default=1,
                     help="heads per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--strong", action="store_true",
+                    help="under torchrun: split the one workload's heads across the ranks (strong scaling) "
+                         "instead of giving every rank a batch of its own (weak scaling, the default)")
+    g = ap.add_argument_group("other modes (their output is not the bench line)")
+    g.add_argument("--sweep", action="store_true", help="throughput over a grid of shapes or named workloads")
+    g.add_argument("--N", type=int, nargs="+", default=[2048, 4096, 8192, 16384, 32768], help="--sweep grid")
+    g.add_argument("--d", type=int, nargs="+", default=[64, 128], help="--sweep grid")
+    g.add_argument("--rows", type=int, default=131072, help="--sweep grid: B*H*N of every shape")
+    g.add_argument("--workloads", nargs="+", choices=sorted(fa_inputs.WORKLOADS), help="--sweep these workloads")
+    g.add_argument("--bwd", action="store_true", help="--sweep / --case: time or run the backward too")
+    g.add_argument("--stepnorm", action="store_true", help="--sweep: also time fa_fwd_stepnorm")
+    g.add_argument("--iters", type=int, default=10, help="--sweep: timed calls per shape; --case: calls")
+    g.add_argument("--case", type=int, nargs=4, metavar=("B", "H", "N", "d"),
+                   help="run one seeded shape --iters times (a fixed command for profilers)")
     args = ap.parse_args()
+    if args.sweep:
+        return run_sweep(args)
+    if args.case:
+        return run_case(args)
     w = fa_inputs.WORKLOADS[args.workload]
     if not w.backward:
         raise SystemExit("the bench step is forward + backward: pick a workload with a backward pass")

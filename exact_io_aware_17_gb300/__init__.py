@@ -19,8 +19,8 @@ FA_OK, FA_ERR_INVALID_ARG, FA_ERR_UNSUPPORTED, FA_ERR_CUDA, FA_ERR_TIMEOUT = ran
 STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3: "FA_ERR_CUDA", 4: "FA_ERR_TIMEOUT"}
 
 # Every symbol include/fa.h declares.
-EXPORTS = ("fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc", "fa_last_error_string",
-           "fa_check_status", "fa_kernel_launches")
+EXPORTS = ("fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc",
+           "fa_last_error_string", "fa_check_status", "fa_kernel_launches", "fa_test_force_wait_timeout")
 
 # Bytes of the static scratch that fa_bwd_noalloc uses (FA_BWD_NOALLOC_MAX_SCRATCH_BYTES).
 NOALLOC_MAX_SCRATCH_BYTES = 32 << 20
@@ -61,6 +61,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_check_status.restype = I
     lib.fa_kernel_launches.argtypes = []
     lib.fa_kernel_launches.restype = ctypes.c_ulonglong
+    lib.fa_test_force_wait_timeout.argtypes = [I]
+    lib.fa_test_force_wait_timeout.restype = None
     _lib = lib
     return lib
 
@@ -196,10 +198,16 @@ def fa_kernel_launches() -> int:
     return int(load_library().fa_kernel_launches())
 
 
+def fa_test_force_wait_timeout(enable: bool) -> None:
+    """Test switch of the failure path: while enabled, the tensor-core kernels withhold their Q loads and
+    their bounded waits run out after ~10 ms (fa_check_status then raises FA_ERR_TIMEOUT).  Tests only."""
+    load_library().fa_test_force_wait_timeout(1 if enable else 0)
+
+
 def fa_last_error_string() -> str:
     return load_library().fa_last_error_string().decode(errors="replace")
 
 
-__all__ = ["fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc", "fa_check_status",
-           "fa_last_error_string",
-           "fa_kernel_launches", "load_library", "FAError", "EXPORTS", "LIB_PATH"]
+__all__ = ["fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc",
+           "fa_check_status", "fa_last_error_string", "fa_kernel_launches", "fa_test_force_wait_timeout",
+           "load_library", "FAError", "EXPORTS", "LIB_PATH"]

@@ -85,10 +85,12 @@ cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, 
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+static std::atomic<int> g_force_wait_timeout{0};
+
 WaitPolicy wait_policy() {
-    const char* v = getenv("FA_TEST_STARVE_WAIT");
-    if (v && v[0] == '1') return WaitPolicy{20000000LL, 1};  // ~10 ms, and the kernels' Q loads withheld
-    return WaitPolicy{4000000000LL, 0};                       // ~2 s: no legitimate wait comes near it
+    if (g_force_wait_timeout.load(std::memory_order_relaxed))
+        return WaitPolicy{20000000LL, 1};  // ~10 ms, and the kernels' Q loads withheld
+    return WaitPolicy{4000000000LL, 0};   // ~2 s: no legitimate wait comes near it
 }
 
 int device_sm_count() {
@@ -129,6 +131,32 @@ static fa_status launch_result(const char* fn, cudaError_t e) {
     return FA_OK;
 }
 
+
+fa_status check_bwd_shape(const char* fn, int B, int H, int N, int d, float scale) {
+    fa_status st = check_shape(fn, B, H, N, d, scale);
+    if (st) return st;
+    if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "%s: d must be 64 or 128 (got %d)", fn, d);
+    return FA_OK;
+}
+
+fa_status bwd_entry(const char* fn, const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+    g_last_error[0] = 0;
+    fa_status st = check_bwd_shape(fn, B, H, N, d, scale);
+    if (st) return st;
+    const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
+    const char* names[] = {"q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv", "workspace"};
+    if ((st = check_ptrs(fn, ptrs, names, 10))) return st;
+    if ((uintptr_t)workspace & 255u) return set_error(FA_ERR_INVALID_ARG, "%s: workspace is not 256-byte aligned", fn);
+    Shape s{B, H, N, d};
+    BwdWorkspace w = bwd_workspace_layout(s);
+    if (workspace_bytes < w.total)
+        return set_error(FA_ERR_INVALID_ARG, "%s: workspace holds %zu bytes, needs %zu", fn, workspace_bytes, w.total);
+    return launch_result(fn, launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, s, scale, workspace,
+                                           (cudaStream_t)stream));
+}
+
 }  // namespace fa
 
 using namespace fa;
@@ -138,6 +166,8 @@ extern "C" {
 const char* fa_last_error_string(void) { return g_last_error; }
 
 unsigned long long fa_kernel_launches(void) { return fa::launch_counter().load(std::memory_order_relaxed); }
+
+void fa_test_force_wait_timeout(int enable) { g_force_wait_timeout.store(enable != 0, std::memory_order_relaxed); }
 
 static fa_status fwd_common(const char* fn, const void* q, const void* k, const void* v, void* o, float* lse, int B,
                             int H, int N, int d, float scale, void* stream, bool stepnorm) {
@@ -185,20 +215,8 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  const float* lse, void* dq, void* dk, void* dv,
                  int B, int H, int N, int d, float scale,
                  void* workspace, size_t workspace_bytes, void* stream) {
-    g_last_error[0] = 0;
-    fa_status st = check_shape("fa_bwd", B, H, N, d, scale);
-    if (st) return st;
-    const void* ptrs[] = {q, k, v, o, dout, lse, dq, dk, dv, workspace};
-    const char* names[] = {"q", "k", "v", "o", "dout", "lse", "dq", "dk", "dv", "workspace"};
-    if ((st = check_ptrs("fa_bwd", ptrs, names, 10))) return st;
-    if ((uintptr_t)workspace & 255u) return set_error(FA_ERR_INVALID_ARG, "fa_bwd: workspace is not 256-byte aligned");
-    if (d != 64 && d != 128) return set_error(FA_ERR_UNSUPPORTED, "fa_bwd: d must be 64 or 128 (got %d)", d);
-    Shape s{B, H, N, d};
-    BwdWorkspace w = bwd_workspace_layout(s);
-    if (workspace_bytes < w.total)
-        return set_error(FA_ERR_INVALID_ARG, "fa_bwd: workspace holds %zu bytes, needs %zu", workspace_bytes, w.total);
-    return launch_result("fa_bwd", launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, s, scale, workspace,
-                                                 (cudaStream_t)stream));
+    return fa::bwd_entry("fa_bwd", q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, workspace, workspace_bytes,
+                         stream);
 }
 
 fa_status fa_check_status(void* stream) {

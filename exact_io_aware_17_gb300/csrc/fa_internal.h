@@ -34,8 +34,9 @@ BwdWorkspace bwd_workspace_layout(const Shape& s);
 // Rows per head of the backward's per-row arrays: N rounded up to the 128-query step of the kernel.
 inline int bwd_padded_rows(int N) { return (N + 127) / 128 * 128; }
 
-// Budget of the kernels' bounded waits, and the test switch that makes the forward's first wait run
-// out (FA_TEST_STARVE_WAIT=1 in the environment: the Q loads are withheld and the budget is ~10 ms).
+// Budget of the kernels' bounded waits (~2 s of clock), and whether the tensor-core kernels withhold their
+// Q loads with a ~10 ms budget so that their first wait runs out.  The latter is only ever set by an
+// explicit fa_test_force_wait_timeout(1) call, which tests of the failure path make.
 struct WaitPolicy {
     long long budget_cycles;
     int starve;
@@ -61,6 +62,13 @@ cudaError_t launch_fwd_simt_f32(const float* q, const float* k, const float* v, 
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                           const float* lse, void* dq, void* dk, void* dv, const Shape& s, float scale,
                           void* workspace, cudaStream_t st);
+
+// Checks of the backward's shape, scale and head size (FA_OK or the error, message recorded with `fn`).
+fa_status check_bwd_shape(const char* fn, int B, int H, int N, int d, float scale);
+// The backward entry point under the name `fn`: every argument check, then the launches.
+fa_status bwd_entry(const char* fn, const void* q, const void* k, const void* v, const void* o, const void* dout,
+                    const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
+                    void* workspace, size_t workspace_bytes, void* stream);
 
 // Adds n to the process-wide count of kernels this library has launched (read by fa_kernel_launches).
 void count_launches(int n);

@@ -16,8 +16,9 @@
  *   - Layout: q, k, v, o, dout, dq, dk, dv are contiguous row-major [B, H, N, d] arrays; lse is a
  *     contiguous [B, H, N] fp32 array.  All pointers are DEVICE pointers, 16-byte aligned.
  *   - Ownership: the caller allocates and frees every buffer (including the backward workspace).
- *     The library allocates no device memory of its own (its one fixed device array is the scratch of
- *     fa_bwd_noalloc) and never anything of N x N size.
+ *     The library allocates no device memory of its own and never anything of N x N size; its only
+ *     fixed device buffers are the static scratch array of fa_bwd_noalloc and one status word per
+ *     kernel source file (read by fa_check_status).
  *   - Streams: `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every
  *     call is asynchronous on that stream; results are valid once the stream has completed.  No call
  *     synchronises the device.
@@ -116,10 +117,15 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  *   Arguments: as fa_bwd, without the workspace.  The call allocates nothing: it uses a scratch array
  *   of FA_BWD_NOALLOC_MAX_SCRATCH_BYTES (32 MiB) compiled into the library, which every GPU that loads
  *   the library holds until the process exits.
+ *   Checks: shape, scale and head size are checked first, exactly as fa_bwd checks them (a d other than
+ *   64 or 128 gives FA_ERR_UNSUPPORTED), then the size of the scratch, then the pointers.
  *   Limit: shapes with fa_bwd_workspace_size(B,H,N,d) > FA_BWD_NOALLOC_MAX_SCRATCH_BYTES are rejected
- *   with FA_ERR_INVALID_ARG before anything is launched (for d = 128: B*H*N above about 64 thousand rows).
+ *   with FA_ERR_INVALID_ARG before anything is launched: for d = 128 (about 520 bytes per row) B*H*N
+ *   above 64528 rows, for d = 64 (about 264 bytes per row) above 127100 rows.  So B=4, H=16, N=2048,
+ *   d=64 (131072 rows) does not fit, nor B=1, H=16, N=8192, d=128; use fa_bwd for those.
  *   Set-up: the first call on a device (made with that device current, like every call) looks up the
- *   array's device address with cudaGetSymbolAddress; make that first call before any stream capture.
+ *   array's device address with cudaGetSymbolAddress, and so does the first call after the device's
+ *   context has changed (for example after cudaDeviceReset); make those calls before any stream capture.
  *   Sharing: all calls on a device share the one array, which keeps the last call's contents (the
  *   kernels clear whatever must start at zero).  Calls whose executions overlap on the GPU (on
  *   different streams, or from different threads) race on the array and give wrong results: order
@@ -129,6 +135,17 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
 fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv,
                          int B, int H, int N, int d, float scale, void* stream);
+
+/*
+ * fa_test_force_wait_timeout — a switch for testing the failure path of the bounded device waits; the
+ * pages have no counterpart.  With enable != 0, every later launch of the tensor-core kernels (fa_fwd,
+ * fa_fwd_stepnorm, fa_bwd, fa_bwd_noalloc, from any thread) withholds its Q tile loads and gives its waits
+ * a budget of about 10 ms instead of about 2 s, so that the first wait on Q runs out: the kernel winds down
+ * by itself (no fault, no trap), fa_check_status() then reports FA_ERR_TIMEOUT, and the outputs of those
+ * calls are not valid.  enable = 0 restores normal operation.  Off by default; nothing but an explicit call
+ * (no environment variable) turns it on.
+ */
+void fa_test_force_wait_timeout(int enable);
 
 /* Message of the last failing call on the calling thread ("" if none).  Valid until the next call. */
 const char* fa_last_error_string(void);

@@ -139,7 +139,8 @@ def backward_rows(q, k, v, do, scale: float, q_rows, k_rows):
     """Gradients at selected rows: dQ at query rows ``q_rows[h]``, dK and dV at key rows ``k_rows[h]``.
 
     dQ_i needs row i of P and dP.  dK_j and dV_j need column j of P and dS, hence every row's softmax
-    statistics (m_i, l_i) and row term, which are formed from the full rows first.
+    statistics (m_i, l_i) and row term, which are formed from the full rows first (a pass over every row
+    that is skipped when no key rows are asked for).
     Returns dq [B,H,Rq,d], dk [B,H,Rk,d], dv [B,H,Rk,d]."""
     q, k, v, do = (np.asarray(t, dtype=np.float64) for t in (q, k, v, do))
     B, H, N, d = q.shape
@@ -154,7 +155,7 @@ def backward_rows(q, k, v, do, scale: float, q_rows, k_rows):
             rb = _row_block(N)
             dk_acc = np.zeros((Rk, d))
             dv_acc = np.zeros((Rk, vh.shape[1]))
-            for r0 in range(0, N, rb):
+            for r0 in range(0, N if Rk else 0, rb):
                 sl = slice(r0, r0 + rb)
                 p, _, _ = softmax_rows(scores(qh[sl], kh, scale))
                 dp = doh[sl] @ vh.T

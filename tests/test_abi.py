@@ -126,3 +126,12 @@ def test_kernel_launch_counter_counts_nothing_without_launches(fa):
     lib = fa.load_library()
     assert lib.fa_fwd(None, None, None, None, None, 1, 1, 8, 64, 0.125, None) == 1   # FA_ERR_INVALID_ARG
     assert fa.fa_kernel_launches() == before
+
+
+def test_test_switch_is_off_by_default_and_ignores_the_environment(fa):
+    """The failure-path switch is an explicit call only: the library source reads no environment variable."""
+    import glob
+    for src in glob.glob(os.path.join(ROOT, "exact_io_aware_17_gb300", "csrc", "*")):
+        assert "getenv" not in open(src).read(), src
+    fa.fa_test_force_wait_timeout(True)
+    fa.fa_test_force_wait_timeout(False)

@@ -283,6 +283,12 @@ def test_rows_forms_match_full():
         np.testing.assert_allclose(sq[:, h], dq[:, h, rows[h]], atol=1e-13)
         np.testing.assert_allclose(sk[:, h], dk[:, h, krows[h]], atol=1e-13)
         np.testing.assert_allclose(sv[:, h], dv[:, h, krows[h]], atol=1e-13)
+    # Query rows only (the pass over every row for dK, dV skipped): the same dQ rows.
+    none = [np.zeros(0, dtype=np.int64)] * H
+    oq, ok_, ov = oracle.backward_rows(q, k, v, do, 0.35, rows, none)
+    assert ok_.shape == (B, H, 0, d) and ov.shape == (B, H, 0, d)
+    for h in range(H):
+        np.testing.assert_allclose(oq[:, h], dq[:, h, rows[h]], atol=1e-13)
 
 
 def test_row_blocking_does_not_change_results(monkeypatch):

@@ -27,6 +27,21 @@ def test_noalloc_rejects_shapes_beyond_the_static_scratch():
     assert "static scratch" in fa.fa_last_error_string()
 
 
+def test_noalloc_checks_the_head_size_before_the_scratch_size():
+    """Host-side check: an unsupported head size is reported as such, under this entry point's name, even
+    for a shape whose scratch would not fit either; nothing is launched."""
+    import exact_io_aware_17_gb300 as fa
+    lib = fa.load_library()
+    fake = [ctypes.c_void_p(0x10000)] * 9
+    launches = fa.fa_kernel_launches()
+    st = lib.fa_bwd_noalloc(*fake, 1, 16, 8192, 96, 0.1, None)
+    assert st == fa.FA_ERR_UNSUPPORTED
+    assert fa.fa_last_error_string().startswith("fa_bwd_noalloc: d must be 64 or 128")
+    st = lib.fa_bwd_noalloc(*fake, 1, 0, 8192, 128, 0.1, None)
+    assert st == fa.FA_ERR_INVALID_ARG and fa.fa_last_error_string().startswith("fa_bwd_noalloc:")
+    assert fa.fa_kernel_launches() == launches
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape", [(2, 4, 1000, 128), (1, 3, 2049, 64)])
 def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row(shape):
@@ -42,12 +57,16 @@ def test_noalloc_matches_fa_bwd_on_two_calls_in_a_row(shape):
     torch.cuda.synchronize()
     torch.cuda.reset_peak_memory_stats()
     before = torch.cuda.memory_allocated()
+    free_before = torch.cuda.mem_get_info()[0]
     for dq, dk, dv in outs:                         # two calls in a row on the shared static scratch
         fa.fa_bwd_noalloc(q, k, v, o, do, lse, scale, dq, dk, dv)
     torch.cuda.synchronize()
     # No torch allocation during the calls: the peak never rose above what was allocated before them
-    # (the current figure may drop if the collector frees an unrelated tensor meanwhile).
+    # (the current figure may drop if the collector frees an unrelated tensor meanwhile) ...
     assert torch.cuda.max_memory_allocated() <= before
+    # ... and no allocation inside the library either: the device's free memory did not shrink (the
+    # static array is part of the module, which was loaded before the first call).
+    assert torch.cuda.mem_get_info()[0] >= free_before
     fa.fa_check_status()
     for got in outs:
         for g, r in zip(got, ref):
