@@ -126,6 +126,9 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
  *   Set-up: the first call on a device (made with that device current, like every call) looks up the
  *   array's device address with cudaGetSymbolAddress, and so does the first call after the device's
  *   context has changed (for example after cudaDeviceReset); make those calls before any stream capture.
+ *   Under CUDA's lazy module loading (the default) that first call is also when the driver loads the
+ *   library's device code and with it the array, so the device's free memory drops by the array's size
+ *   then, and never again; a caller that must not see that happen later makes the set-up call early.
  *   Sharing: all calls on a device share the one array, which keeps the last call's contents (the
  *   kernels clear whatever must start at zero).  Calls whose executions overlap on the GPU (on
  *   different streams, or from different threads) race on the array and give wrong results: order
