@@ -5,6 +5,7 @@
 #include <math.h>
 
 #include <atomic>
+#include <mutex>
 #include <stdlib.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -56,8 +57,75 @@ static cudaError_t tmap_encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
     return cudaSuccess;
 }
 
+// Encoded tensor maps, keyed by everything that goes into them (a map holds the array's address, its shape
+// and the box, nothing of the device or context), so that repeated calls on the same buffers skip the
+// driver's encoding.  A small table with round-robin replacement, shared by all threads.
+namespace {
+struct TmapKey {
+    const void* base;
+    int64_t heads;
+    int d, N, box_cols, box_rows, dtype;
+    bool operator==(const TmapKey& o) const {
+        return base == o.base && heads == o.heads && d == o.d && N == o.N && box_cols == o.box_cols &&
+               box_rows == o.box_rows && dtype == o.dtype;
+    }
+};
+constexpr int kTmapCacheSize = 64;
+struct TmapEntry {
+    bool used;
+    TmapKey key;
+    CUtensorMap map;
+};
+TmapEntry g_tmap_cache[kTmapCacheSize];
+int g_tmap_next = 0;
+std::mutex g_tmap_mu;
+
+bool tmap_lookup(const TmapKey& k, CUtensorMap* out) {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    for (const TmapEntry& e : g_tmap_cache)
+        if (e.used && e.key == k) {
+            *out = e.map;
+            return true;
+        }
+    return false;
+}
+
+void tmap_store(const TmapKey& k, const CUtensorMap& map) {
+    std::lock_guard<std::mutex> lock(g_tmap_mu);
+    TmapEntry& e = g_tmap_cache[g_tmap_next];
+    g_tmap_next = (g_tmap_next + 1) % kTmapCacheSize;
+    e.used = true;
+    e.key = k;
+    e.map = map;
+}
+}  // namespace
+
+cudaError_t set_max_dynamic_smem(const void* func, int bytes) {
+    // The limit set so far per kernel and device: the attribute call is made only to raise it.
+    static std::mutex mu;
+    static struct {
+        const void* func;
+        int dev, bytes;
+    } set[256];
+    static int n_set = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(mu);
+    int i = 0;
+    while (i < n_set && !(set[i].func == func && set[i].dev == dev)) ++i;
+    if (i < n_set && set[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess) return e;
+    if (i < n_set) set[i].bytes = bytes;
+    else if (n_set < 256) set[n_set++] = {func, dev, bytes};
+    return cudaSuccess;
+}
+
 cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int d, int N, int64_t heads, int box_cols,
                              int box_rows) {
+    const TmapKey key{base, heads, d, N, box_cols, box_rows, 1};
+    if (tmap_lookup(key, map)) return cudaSuccess;
     PFN_cuTensorMapEncodeTiled_v12000 encode;
     cudaError_t e = tmap_encoder(&encode);
     if (e != cudaSuccess) return e;
@@ -68,10 +136,14 @@ cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int d, int N, 
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    tmap_store(key, *map);
+    return cudaSuccess;
 }
 
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows) {
+    const TmapKey key{base, heads, d, N, 64, box_rows, 0};
+    if (tmap_lookup(key, map)) return cudaSuccess;
     PFN_cuTensorMapEncodeTiled_v12000 encode;
     cudaError_t e = tmap_encoder(&encode);
     if (e != cudaSuccess) return e;
@@ -82,7 +154,9 @@ cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, 
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    tmap_store(key, *map);
+    return cudaSuccess;
 }
 
 static std::atomic<int> g_force_wait_timeout{0};

@@ -703,7 +703,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     if ((e = make_tmap_bf16_3d(&tk, k, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
     if ((e = make_tmap_f32_3d(&tdq, dq_acc, s.d, s.N, s.heads(), 32, HQ)) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(bwd_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    e = set_max_dynamic_smem((const void*)bwd_tc_kernel<D>, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int bph = (s.N + BK - 1) / BK;
     if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;

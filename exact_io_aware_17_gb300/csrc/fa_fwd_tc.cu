@@ -599,7 +599,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
     if ((e = make_tmap_bf16_3d(&tq, q, s.d, s.N, s.heads(), BM)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tk, k, s.d, s.N, s.heads(), BN)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BN)) != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fwd_tc_kernel<D, kStepNorm>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmemBytes);
+    e = set_max_dynamic_smem((const void*)fwd_tc_kernel<D, kStepNorm>, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int bph = (s.N + 2 * BM - 1) / (2 * BM);
     if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;

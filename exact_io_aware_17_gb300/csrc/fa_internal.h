@@ -46,8 +46,13 @@ WaitPolicy wait_policy();
 // Multiprocessor count of the current device (cached per device).
 int device_sm_count();
 
+// Makes a kernel's dynamic shared-memory limit on the current device at least `bytes` (the attribute call is
+// made only when the limit has to rise).
+cudaError_t set_max_dynamic_smem(const void* func, int bytes);
+
 // Encodes a TMA descriptor for a bf16 [heads, N, d] array (d innermost) with boxes of 64 columns x
-// `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.
+// `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.  Encoded maps are cached by
+// their arguments (address, shape, box), so repeated calls on the same buffers cost a table lookup.
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows);
 // fp32 [heads][N][d] viewed as (d, N, heads), unswizzled boxes of box_cols x box_rows (box_cols * 4 bytes a
 // multiple of 16): the dQ accumulator as the target of tensor reduce-adds.

@@ -148,9 +148,10 @@ cudaError_t launch_fwd(const T* q, const T* k, const T* v, T* o, float* lse, con
     if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
     const unsigned grid = (unsigned)(bph * s.heads());
     size_t smem = sizeof(float) * (2 * kBlk * (s.d + 1) + kWarps * kRows * s.d);
-    cudaFuncSetAttribute(fwd_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = set_max_dynamic_smem((const void*)fwd_simt_kernel<T>, (int)smem);
+    if (e != cudaSuccess) return e;
     fwd_simt_kernel<T><<<grid, kWarps * 32, smem, st>>>(q, k, v, o, lse, s.N, s.d, bph, scale);
-    const cudaError_t e = cudaGetLastError();
+    e = cudaGetLastError();
     if (e == cudaSuccess) count_launches(1);
     return e;
 }
