@@ -240,6 +240,12 @@ def run_ours(args, w):
     fa.fa_check_status(stream)
 
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    # The backward's main kernel alone, between events the library records around it (fa_debug_time_bwd_main);
+    # each event is recorded once first so that it exists.
+    evm = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+    for pair in evm:
+        for e in pair:
+            e.record(stream)
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -254,6 +260,7 @@ def run_ours(args, w):
         ev[i][0].record(stream)
         fa.fa_fwd(q, k, v, w.scale, o, lse, stream=stream)
         ev[i][1].record(stream)
+        fa.fa_debug_time_bwd_main(evm[i][0], evm[i][1])
         fa.fa_bwd(q, k, v, o, do, lse, w.scale, dq, dk, dv, ws, stream=stream)
         ev[i][2].record(stream)
     torch.cuda.synchronize()
@@ -267,6 +274,7 @@ def run_ours(args, w):
 
     fwd_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     bwd_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    main_ms = [evm[i][0].elapsed_time(evm[i][1]) for i in range(args.steps)]
     step_ms = sum(fwd_ms) / args.steps + sum(bwd_ms) / args.steps
     step_ms = max_over_ranks(step_ms, dev)
     # Work of this rank's heads, and of the whole job (all ranks) per step.
@@ -299,10 +307,11 @@ def run_ours(args, w):
         "e2e": {"value": total_flops / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "ms_per_step": e2e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "how": "pinned host q,k,v,dO copied in and o,lse,dq,dk,dv copied out every step, through the "
-                       "public API; copies run on two copy streams, double-buffered so that step i's "
-                       "transfers overlap steps i-1 and i+1's compute"},
+                       "public API; one copy stream per tensor, double-buffered so that step i's transfers "
+                       "overlap steps i-1 and i+1's compute"},
     }
-    line["roofline"] = _roofline(lw if strong else w, fwd_avg, bwd_avg, peaks)
+    line["bwd"]["main_kernel_ms"] = sum(main_ms) / args.steps
+    line["roofline"] = _roofline(lw, fwd_avg, bwd_avg, sum(main_ms) / args.steps, peaks, whole_workload=not strong)
     line["exp_pipe"] = _exp_pipe(lw, fwd_avg, bwd_avg)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         f, t = _oracle_sample(w, args.oracle_heads, inp_cpu)
@@ -317,54 +326,67 @@ def run_ours(args, w):
 
 
 def _e2e(fa, w, inp_cpu, dev, steps):
-    """Per-step time of fa_fwd + fa_bwd fed from and drained to pinned host memory (double-buffered)."""
+    """Per-step time of fa_fwd + fa_bwd fed from and drained to pinned host memory, double-buffered: step i's
+    inputs are copied in while step i-1 computes, and its outputs copied out while step i+1 computes.  Every
+    tensor has a copy stream of its own, so that the copies of a step use several copy engines at once."""
     B, H, N, d = w.B, w.H, w.N, w.d
-    host_in = {n: inp_cpu[n].pin_memory() for n in ("q", "k", "v", "do")}
+    ins, outs = ("q", "k", "v", "do"), ("o", "lse", "dq", "dk", "dv")
+    host_in = {n: inp_cpu[n].pin_memory() for n in ins}
     host_out = [{n: torch.empty(B, H, N, d, dtype=inp_cpu["q"].dtype).pin_memory() for n in ("o", "dq", "dk", "dv")}
                 for _ in range(2)]
     for h in host_out:
         h["lse"] = torch.empty(B, H, N, dtype=torch.float32).pin_memory()
     bufs = []
     for _ in range(2):
-        b = {n: torch.empty(B, H, N, d, dtype=inp_cpu["q"].dtype, device=dev) for n in ("q", "k", "v", "do", "o", "dq", "dk", "dv")}
+        b = {n: torch.empty(B, H, N, d, dtype=inp_cpu["q"].dtype, device=dev) for n in ins + ("o", "dq", "dk", "dv")}
         b["lse"] = torch.empty(B, H, N, dtype=torch.float32, device=dev)
         b["ws"] = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=dev)
         bufs.append(b)
     comp = torch.cuda.current_stream(dev)
-    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    free = [torch.cuda.Event() for _ in range(2)]
-    loaded = [torch.cuda.Event() for _ in range(2)]
-    computed = [torch.cuda.Event() for _ in range(2)]
-    for e in free:
-        e.record(comp)
+    s_in = {n: torch.cuda.Stream(dev) for n in ins}
+    s_out = {n: torch.cuda.Stream(dev) for n in outs}
+    computed = [torch.cuda.Event() for _ in range(2)]          # buffer j's inputs read, outputs written
+    loaded = [{n: torch.cuda.Event() for n in ins} for _ in range(2)]
+    drained = [{n: torch.cuda.Event() for n in outs} for _ in range(2)]
+    for j in range(2):
+        computed[j].record(comp)
+        for e in drained[j].values():
+            e.record(comp)
 
     def run(n):
         for i in range(n):
             j = i % 2
             b, ho = bufs[j], host_out[j]
-            h2d_s.wait_event(free[j])
-            with torch.cuda.stream(h2d_s):
-                for name in ("q", "k", "v", "do"):
+            for name in ins:                               # buffer j's inputs are free once step i-2 computed
+                st = s_in[name]
+                st.wait_event(computed[j])
+                with torch.cuda.stream(st):
                     b[name].copy_(host_in[name], non_blocking=True)
-                loaded[j].record(h2d_s)
-            comp.wait_event(loaded[j])
+                    loaded[j][name].record(st)
+            for name in ins:
+                comp.wait_event(loaded[j][name])
+            for name in outs:                              # ... and its outputs once step i-2's were copied out
+                comp.wait_event(drained[j][name])
             fa.fa_fwd(b["q"], b["k"], b["v"], w.scale, b["o"], b["lse"], stream=comp)
             fa.fa_bwd(b["q"], b["k"], b["v"], b["o"], b["do"], b["lse"], w.scale, b["dq"], b["dk"], b["dv"], b["ws"],
                       stream=comp)
             computed[j].record(comp)
-            d2h_s.wait_event(computed[j])
-            with torch.cuda.stream(d2h_s):
-                for name in ("o", "lse", "dq", "dk", "dv"):
+            for name in outs:
+                st = s_out[name]
+                st.wait_event(computed[j])
+                with torch.cuda.stream(st):
                     ho[name].copy_(b[name], non_blocking=True)
-                free[j].record(d2h_s)
+                    drained[j][name].record(st)
 
     run(4)
     torch.cuda.synchronize(dev)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(comp)
-    h2d_s.wait_stream(comp)
+    for st in list(s_in.values()) + list(s_out.values()):
+        st.wait_stream(comp)
     run(steps)
-    comp.wait_stream(d2h_s)
+    for st in s_out.values():
+        comp.wait_stream(st)
     end.record(comp)
     torch.cuda.synchronize(dev)
     elt = inp_cpu["q"].element_size() * inp_cpu["q"].numel()
@@ -418,17 +440,21 @@ def _exp_pipe(w, fwd_ms, bwd_ms):
             "frac_bwd": bwd / EX2_PER_S, "peak_source": "measured (ex2.approx throughput microbenchmark)"}
 
 
-def _roofline(w, fwd_ms, bwd_ms, peaks):
-    """Roofline of the dominant kernel (the one with the larger share of the step)."""
+def _roofline(w, fwd_ms, bwd_ms, main_ms, peaks, whole_workload=True):
+    """Roofline of the dominant kernel: the backward's main kernel (bwd_tc_kernel), whose time the library
+    records between events around its launch, unless the forward takes longer.  Achieved = the kernel's
+    algorithmic flops (10*B*H*N^2*d: the five N x N x d products) / its average event-timed duration."""
     if bwd_ms >= fwd_ms:
-        name, flops, ms = "backward", w.bwd_flops(), bwd_ms
+        name, flops, ms = "backward", w.bwd_flops(), main_ms
+        kernel = "bwd_tc_kernel (the backward's main kernel, timed alone between library-recorded events)"
     else:
         name, flops, ms = "forward", w.fwd_flops(), fwd_ms
+        kernel = "fwd_tc_kernel (the forward's launches)"
     achieved = flops / (ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"]
-    traffic, source = _traffic(name, w)
-    return {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-            "frac": achieved / peak, "peak_source": f"{peaks['source']} burst bf16 (cuBLAS)",
+    traffic, source = _traffic(name, w) if whole_workload else (None, "no capture for a rank's share of the heads")
+    return {"kernel": kernel, "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "ms_per_launch": ms, "peak_source": f"{peaks['source']} burst bf16 (cuBLAS)",
             "traffic": traffic, "traffic_unit": "DRAM bytes per launch of the main kernel", "traffic_source": source}
 
 

@@ -20,7 +20,8 @@ STATUS_NAMES = {0: "FA_OK", 1: "FA_ERR_INVALID_ARG", 2: "FA_ERR_UNSUPPORTED", 3:
 
 # Every symbol include/fa.h declares.
 EXPORTS = ("fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd_workspace_size", "fa_bwd", "fa_bwd_noalloc",
-           "fa_last_error_string", "fa_check_status", "fa_kernel_launches", "fa_test_force_wait_timeout")
+           "fa_last_error_string", "fa_check_status", "fa_kernel_launches", "fa_test_force_wait_timeout",
+           "fa_debug_time_bwd_main")
 
 # Bytes of the static scratch that fa_bwd_noalloc uses (FA_BWD_NOALLOC_MAX_SCRATCH_BYTES).
 NOALLOC_MAX_SCRATCH_BYTES = 32 << 20
@@ -61,6 +62,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.fa_check_status.restype = I
     lib.fa_kernel_launches.argtypes = []
     lib.fa_kernel_launches.restype = ctypes.c_ulonglong
+    lib.fa_debug_time_bwd_main.argtypes = [P, P]
+    lib.fa_debug_time_bwd_main.restype = None
     lib.fa_test_force_wait_timeout.argtypes = [I]
     lib.fa_test_force_wait_timeout.restype = None
     _lib = lib
@@ -198,6 +201,12 @@ def fa_kernel_launches() -> int:
     return int(load_library().fa_kernel_launches())
 
 
+def fa_debug_time_bwd_main(start, stop) -> None:
+    """Timing diagnostic: the next fa_bwd / fa_bwd_noalloc on this thread records the torch.cuda.Events
+    `start` and `stop` (already recorded once, so that they exist) around its main kernel only."""
+    load_library().fa_debug_time_bwd_main(ctypes.c_void_p(start.cuda_event), ctypes.c_void_p(stop.cuda_event))
+
+
 def fa_test_force_wait_timeout(enable: bool) -> None:
     """Test switch of the failure path: while enabled, the tensor-core kernels withhold their Q loads and
     their bounded waits run out after ~10 ms (fa_check_status then raises FA_ERR_TIMEOUT).  Tests only."""
@@ -210,4 +219,4 @@ def fa_last_error_string() -> str:
 
 __all__ = ["fa_fwd", "fa_fwd_stepnorm", "fa_fwd_f32", "fa_bwd", "fa_bwd_workspace_size", "fa_bwd_noalloc",
            "fa_check_status", "fa_last_error_string", "fa_kernel_launches", "fa_test_force_wait_timeout",
-           "load_library", "FAError", "EXPORTS", "LIB_PATH"]
+           "fa_debug_time_bwd_main", "load_library", "FAError", "EXPORTS", "LIB_PATH"]

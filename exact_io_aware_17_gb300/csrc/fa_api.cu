@@ -15,6 +15,13 @@
 namespace fa {
 
 static thread_local char g_last_error[512] = "";
+static thread_local cudaEvent_t g_bwd_main_events[2] = {nullptr, nullptr};
+
+void take_bwd_main_events(cudaEvent_t* start, cudaEvent_t* stop) {
+    *start = g_bwd_main_events[0];
+    *stop = g_bwd_main_events[1];
+    g_bwd_main_events[0] = g_bwd_main_events[1] = nullptr;
+}
 
 fa_status set_error(fa_status st, const char* fmt, ...) {
     va_list ap;
@@ -240,6 +247,11 @@ extern "C" {
 const char* fa_last_error_string(void) { return g_last_error; }
 
 unsigned long long fa_kernel_launches(void) { return fa::launch_counter().load(std::memory_order_relaxed); }
+
+void fa_debug_time_bwd_main(void* start_event, void* stop_event) {
+    g_bwd_main_events[0] = (cudaEvent_t)start_event;
+    g_bwd_main_events[1] = (cudaEvent_t)stop_event;
+}
 
 void fa_test_force_wait_timeout(int enable) { g_force_wait_timeout.store(enable != 0, std::memory_order_relaxed); }
 

@@ -709,11 +709,15 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
     const unsigned grid = (unsigned)(bph * s.heads());
     const WaitPolicy wp = wait_policy();
+    cudaEvent_t ev_start, ev_stop;
+    take_bwd_main_events(&ev_start, &ev_stop);
+    if (ev_start && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
     bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse2, row_d, dq_acc,
                                                             (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, s.N, Npad, bph, scale,
                                                             scale * 1.4426950408889634f, wp.budget_cycles, wp.starve);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     count_launches(1);
+    if (ev_stop && (e = cudaEventRecord(ev_stop, st)) != cudaSuccess) return e;
     bwd_dq_convert_kernel<<<blocks, 256, 0, st>>>(dq_acc, (__nv_bfloat16*)dq, scale, s.heads() * (int64_t)s.N * D / 4);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     count_launches(1);

@@ -75,6 +75,10 @@ fa_status bwd_entry(const char* fn, const void* q, const void* k, const void* v,
                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
                     void* workspace, size_t workspace_bytes, void* stream);
 
+// Events that the next backward on this thread records around its main kernel (both null: none); taking them
+// clears them (fa_debug_time_bwd_main).
+void take_bwd_main_events(cudaEvent_t* start, cudaEvent_t* stop);
+
 // Adds n to the process-wide count of kernels this library has launched (read by fa_kernel_launches).
 void count_launches(int n);
 std::atomic<unsigned long long>& launch_counter();

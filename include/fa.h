@@ -140,6 +140,16 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
                          int B, int H, int N, int d, float scale, void* stream);
 
 /*
+ * fa_debug_time_bwd_main — a timing diagnostic; the pages have no counterpart.  The next fa_bwd or
+ * fa_bwd_noalloc call made on the calling thread records `start_event` on its stream right before the
+ * backward's main kernel (the one that forms P, dS, dV, dK and dQ) and `stop_event` right after it, so that
+ * cudaEventElapsedTime gives that kernel's time alone (the call's other two kernels, the row terms before it
+ * and the dQ conversion after it, are outside).  Both are cudaEvent_t passed as void*, created by the
+ * caller on the call's device; the setting is used once (that call clears it); NULL, NULL clears it.
+ */
+void fa_debug_time_bwd_main(void* start_event, void* stop_event);
+
+/*
  * fa_test_force_wait_timeout — a switch for testing the failure path of the bounded device waits; the
  * pages have no counterpart.  With enable != 0, every later launch of the tensor-core kernels (fa_fwd,
  * fa_fwd_stepnorm, fa_bwd, fa_bwd_noalloc, from any thread) withholds its Q tile loads and gives its waits

@@ -277,3 +277,29 @@ def test_bwd_rejects_bad_caller_outputs_and_workspace():
             fa.fa_bwd_noalloc(q, k, v, o, do, lse, **kw)
     torch.cuda.synchronize()
     assert fa.fa_kernel_launches() == launches    # nothing was launched
+
+
+def test_main_kernel_timing_events_are_recorded_once():
+    """fa_debug_time_bwd_main: the next backward records the two events around its main kernel only (a
+    positive time below the whole call's), and the setting is used once."""
+    fa = need_gpu()
+    B, H, N, d = 1, 8, 4096, 128
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed=81, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fa_fwd(q, k, v)
+    stream = torch.cuda.current_stream()
+    e0, e1, a, b = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    for e in (e0, e1):
+        e.record(stream)
+    torch.cuda.synchronize()
+    fa.fa_debug_time_bwd_main(e0, e1)
+    a.record(stream)
+    fa.fa_bwd(q, k, v, o, do, lse)
+    b.record(stream)
+    torch.cuda.synchronize()
+    main_ms, call_ms = e0.elapsed_time(e1), a.elapsed_time(b)
+    assert 0 < main_ms < call_ms
+    fa.fa_bwd(q, k, v, o, do, lse)            # the setting was used once: these events stay as they were
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) == main_ms
+    fa.fa_check_status()
