@@ -399,11 +399,11 @@ def _e2e(fa, w, inp_cpu, dev, steps):
 # stale: the JSON line then reports traffic null and says so.
 TRAFFIC = {
     ("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): {
-        "bytes": 202915584 + 83937024,
+        "bytes": 202718208 + 83671296,
         "profile": "profiles/dram_per_launch_bench_B1-H16-N8192-d128.md",
         "kernel": "bwd_tc_kernel<128>",
         "sources": ("exact_io_aware_17_gb300/csrc/fa_bwd_tc.cu", "exact_io_aware_17_gb300/csrc/fa_ptx.cuh"),
-        "sha256": "02ca527aed86d07f37ec5cd5667d5a69f4cbf45bbe319c147f3efe44b7eec991",
+        "sha256": "d1150f1751da1a97c04533e42ecbbf0bf0c2fa2fc7b7b3d5b75c4688c737df0d",
     },
 }
 
