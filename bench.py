@@ -514,6 +514,13 @@ def run_sweep(args):
         if args.stepnorm:
             tsn = _time_call(lambda: fa.fa_fwd_stepnorm(t["q"], t["k"], t["v"], w.scale, o, lse), flush, args.iters)
             line.update(stepnorm_fwd_ms=tsn, stepnorm_fwd_tflops=w.fwd_flops() / tsn / 1e9, stepnorm_slowdown=tsn / tf)
+        if args.f32:
+            # The fp32 CUDA-core forward on the same values (the bf16 inputs widened to fp32).
+            q32, k32, v32 = (t[n].float() for n in ("q", "k", "v"))
+            o32, l32 = fa.fa_fwd_f32(q32, k32, v32, w.scale)
+            t32 = _time_call(lambda: fa.fa_fwd_f32(q32, k32, v32, w.scale, o32, l32), flush, args.iters)
+            line.update(f32_fwd_ms=t32, f32_fwd_tflops=w.fwd_flops() / t32 / 1e9)
+            del q32, k32, v32, o32, l32
         fa.fa_check_status()
         line.update(peak_tflops=peak, peak_source=peaks["source"])
         print(json.dumps(line), flush=True)
@@ -563,6 +570,7 @@ def main():
     g.add_argument("--workloads", nargs="+", choices=sorted(fa_inputs.WORKLOADS), help="--sweep these workloads")
     g.add_argument("--bwd", action="store_true", help="--sweep / --case: time or run the backward too")
     g.add_argument("--stepnorm", action="store_true", help="--sweep: also time fa_fwd_stepnorm")
+    g.add_argument("--f32", action="store_true", help="--sweep: also time the fp32 forward fa_fwd_f32")
     g.add_argument("--iters", type=int, default=10, help="--sweep: timed calls per shape; --case: calls")
     g.add_argument("--case", type=int, nargs=4, metavar=("B", "H", "N", "d"),
                    help="run one seeded shape --iters times (a fixed command for profilers)")
