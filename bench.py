@@ -427,7 +427,8 @@ def _traffic(name, w):
 
 
 # Measured throughput of the exponential unit (ex2.approx.f32, whole GPU), the second ceiling of the
-# softmax work: `python -m exact_io_aware_17_gb300.mufu_peak` on this GPU model.
+# softmax work: a recorded result of a standalone microbenchmark on this GPU model
+# (profiles/mufu_ex2_peak.md).
 EX2_PER_S = 9.97e12
 
 
