@@ -17,10 +17,10 @@ namespace fa {
 static thread_local char g_last_error[512] = "";
 static thread_local cudaEvent_t g_bwd_main_events[2] = {nullptr, nullptr};
 
-void take_bwd_main_events(cudaEvent_t* start, cudaEvent_t* stop) {
-    *start = g_bwd_main_events[0];
-    *stop = g_bwd_main_events[1];
+BwdTiming take_bwd_main_events() {
+    const BwdTiming t{g_bwd_main_events[0], g_bwd_main_events[1]};
     g_bwd_main_events[0] = g_bwd_main_events[1] = nullptr;
+    return t;
 }
 
 fa_status set_error(fa_status st, const char* fmt, ...) {
@@ -222,7 +222,7 @@ fa_status check_bwd_shape(const char* fn, int B, int H, int N, int d, float scal
 
 fa_status bwd_entry(const char* fn, const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
-                    void* workspace, size_t workspace_bytes, void* stream) {
+                    void* workspace, size_t workspace_bytes, void* stream, BwdTiming timing) {
     g_last_error[0] = 0;
     fa_status st = check_bwd_shape(fn, B, H, N, d, scale);
     if (st) return st;
@@ -235,7 +235,7 @@ fa_status bwd_entry(const char* fn, const void* q, const void* k, const void* v,
     if (workspace_bytes < w.total)
         return set_error(FA_ERR_INVALID_ARG, "%s: workspace holds %zu bytes, needs %zu", fn, workspace_bytes, w.total);
     return launch_result(fn, launch_bwd_tc(q, k, v, o, dout, lse, dq, dk, dv, s, scale, workspace,
-                                           (cudaStream_t)stream));
+                                           (cudaStream_t)stream, timing));
 }
 
 }  // namespace fa
@@ -302,7 +302,7 @@ fa_status fa_bwd(const void* q, const void* k, const void* v, const void* o, con
                  int B, int H, int N, int d, float scale,
                  void* workspace, size_t workspace_bytes, void* stream) {
     return fa::bwd_entry("fa_bwd", q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, workspace, workspace_bytes,
-                         stream);
+                         stream, fa::take_bwd_main_events());
 }
 
 fa_status fa_check_status(void* stream) {

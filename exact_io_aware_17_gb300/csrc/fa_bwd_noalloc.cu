@@ -77,6 +77,7 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
                                     float scale, void* stream) {
     using namespace fa;
     static const char* kFn = "fa_bwd_noalloc";
+    const BwdTiming timing = take_bwd_main_events();
     fa_status st = check_bwd_shape(kFn, B, H, N, d, scale);
     if (st) return st;
     const size_t need = fa_bwd_workspace_size(B, H, N, d);
@@ -93,5 +94,5 @@ extern "C" fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v,
     // The backward checks every other argument and clears, before use, every part of the scratch that
     // must start at zero.
     return bwd_entry(kFn, q, k, v, o, dout, lse, dq, dk, dv, B, H, N, d, scale, scratch, kNoallocScratchBytes,
-                     stream);
+                     stream, timing);
 }

@@ -682,7 +682,8 @@ __global__ void bwd_dq_convert_kernel(const float* __restrict__ dq_acc, __nv_bfl
 
 template <int D>
 cudaError_t launch(const void* q, const void* k, const void* v, const void* o, const void* dout, const float* lse,
-                   void* dq, void* dk, void* dv, const Shape& s, float scale, void* workspace, cudaStream_t st) {
+                   void* dq, void* dk, void* dv, const Shape& s, float scale, void* workspace, cudaStream_t st,
+                   BwdTiming timing) {
     using C = BwdCfg<D>;
     const BwdWorkspace w = bwd_workspace_layout(s);
     char* ws = (char*)workspace;
@@ -709,15 +710,13 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     if ((long long)bph * s.heads() > INT32_MAX) return cudaErrorInvalidConfiguration;
     const unsigned grid = (unsigned)(bph * s.heads());
     const WaitPolicy wp = wait_policy();
-    cudaEvent_t ev_start, ev_stop;
-    take_bwd_main_events(&ev_start, &ev_stop);
-    if (ev_start && (e = cudaEventRecord(ev_start, st)) != cudaSuccess) return e;
+    if (timing.start && (e = cudaEventRecord(timing.start, st)) != cudaSuccess) return e;
     bwd_tc_kernel<D><<<grid, kThreads, C::kSmemBytes, st>>>(tq, tk, tv, tdo, tdq, lse2, row_d, dq_acc,
                                                             (__nv_bfloat16*)dk, (__nv_bfloat16*)dv, s.N, Npad, bph, scale,
                                                             scale * 1.4426950408889634f, wp.budget_cycles, wp.starve);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     count_launches(1);
-    if (ev_stop && (e = cudaEventRecord(ev_stop, st)) != cudaSuccess) return e;
+    if (timing.stop && (e = cudaEventRecord(timing.stop, st)) != cudaSuccess) return e;
     bwd_dq_convert_kernel<<<blocks, 256, 0, st>>>(dq_acc, (__nv_bfloat16*)dq, scale, s.heads() * (int64_t)s.N * D / 4);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     count_launches(1);
@@ -728,9 +727,9 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
 
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                           const float* lse, void* dq, void* dk, void* dv, const Shape& s, float scale,
-                          void* workspace, cudaStream_t st) {
-    return s.d == 128 ? launch<128>(q, k, v, o, dout, lse, dq, dk, dv, s, scale, workspace, st)
-                      : launch<64>(q, k, v, o, dout, lse, dq, dk, dv, s, scale, workspace, st);
+                          void* workspace, cudaStream_t st, BwdTiming timing) {
+    return s.d == 128 ? launch<128>(q, k, v, o, dout, lse, dq, dk, dv, s, scale, workspace, st, timing)
+                      : launch<64>(q, k, v, o, dout, lse, dq, dk, dv, s, scale, workspace, st, timing);
 }
 
 int bwd_tc_read_and_clear_status(cudaStream_t st) {

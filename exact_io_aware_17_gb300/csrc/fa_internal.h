@@ -64,20 +64,25 @@ cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, 
                           float scale, cudaStream_t st, bool stepnorm);
 cudaError_t launch_fwd_simt_f32(const float* q, const float* k, const float* v, float* o, float* lse,
                                 const Shape& s, float scale, cudaStream_t st);
+// Events recorded around the backward's main kernel (both null: none), see fa_debug_time_bwd_main.
+struct BwdTiming {
+    cudaEvent_t start, stop;
+};
 cudaError_t launch_bwd_tc(const void* q, const void* k, const void* v, const void* o, const void* dout,
                           const float* lse, void* dq, void* dk, void* dv, const Shape& s, float scale,
-                          void* workspace, cudaStream_t st);
+                          void* workspace, cudaStream_t st, BwdTiming timing);
 
 // Checks of the backward's shape, scale and head size (FA_OK or the error, message recorded with `fn`).
 fa_status check_bwd_shape(const char* fn, int B, int H, int N, int d, float scale);
 // The backward entry point under the name `fn`: every argument check, then the launches.
 fa_status bwd_entry(const char* fn, const void* q, const void* k, const void* v, const void* o, const void* dout,
                     const float* lse, void* dq, void* dk, void* dv, int B, int H, int N, int d, float scale,
-                    void* workspace, size_t workspace_bytes, void* stream);
+                    void* workspace, size_t workspace_bytes, void* stream, BwdTiming timing);
 
-// Events that the next backward on this thread records around its main kernel (both null: none); taking them
-// clears them (fa_debug_time_bwd_main).
-void take_bwd_main_events(cudaEvent_t* start, cudaEvent_t* stop);
+// The events that the calling thread's next backward call records around its main kernel (both null:
+// none); taking them clears them, so each backward entry point takes them first, whether it then launches
+// or fails its checks (fa_debug_time_bwd_main).
+BwdTiming take_bwd_main_events();
 
 // Adds n to the process-wide count of kernels this library has launched (read by fa_kernel_launches).
 void count_launches(int n);

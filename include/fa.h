@@ -145,7 +145,8 @@ fa_status fa_bwd_noalloc(const void* q, const void* k, const void* v, const void
  * backward's main kernel (the one that forms P, dS, dV, dK and dQ) and `stop_event` right after it, so that
  * cudaEventElapsedTime gives that kernel's time alone (the call's other two kernels, the row terms before it
  * and the dQ conversion after it, are outside).  Both are cudaEvent_t passed as void*, created by the
- * caller on the call's device; the setting is used once (that call clears it); NULL, NULL clears it.
+ * caller on the call's device.  The setting is used once: the next backward call takes it even if that
+ * call then fails its argument checks (and so records nothing).  NULL, NULL clears it.
  */
 void fa_debug_time_bwd_main(void* start_event, void* stop_event);
 

@@ -135,3 +135,15 @@ def test_test_switch_is_off_by_default_and_ignores_the_environment(fa):
         assert "getenv" not in open(src).read(), src
     fa.fa_test_force_wait_timeout(True)
     fa.fa_test_force_wait_timeout(False)
+
+
+def test_timing_request_is_consumed_by_a_backward_that_fails_its_checks(fa):
+    """fa_debug_time_bwd_main is one-shot: the next backward call takes it even when it then fails its
+    argument checks, so a stale request never attaches to a later call (host only: nothing is launched)."""
+    lib = fa.load_library()
+    ptrs = [FAKE] * 9
+    lib.fa_debug_time_bwd_main(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))   # never recorded
+    launches = fa.fa_kernel_launches()
+    assert lib.fa_bwd(*ptrs, 1, 1, 0, 64, 0.125, FAKE, 1 << 20, None) == fa.FA_ERR_INVALID_ARG
+    assert lib.fa_bwd_noalloc(*ptrs, 1, 1, 0, 64, 0.125, None) == fa.FA_ERR_INVALID_ARG
+    assert fa.fa_kernel_launches() == launches
