@@ -137,9 +137,9 @@ def test_test_switch_is_off_by_default_and_ignores_the_environment(fa):
     fa.fa_test_force_wait_timeout(False)
 
 
-def test_timing_request_is_consumed_by_a_backward_that_fails_its_checks(fa):
-    """fa_debug_time_bwd_main is one-shot: the next backward call takes it even when it then fails its
-    argument checks, so a stale request never attaches to a later call (host only: nothing is launched)."""
+def test_pending_timing_request_changes_no_argument_check(fa):
+    """With a fa_debug_time_bwd_main request pending, rejected backward calls still fail their checks before
+    anything is launched (host only; that they also consume the request is checked on the GPU)."""
     lib = fa.load_library()
     ptrs = [FAKE] * 9
     lib.fa_debug_time_bwd_main(ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000))   # never recorded

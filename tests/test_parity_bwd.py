@@ -302,4 +302,12 @@ def test_main_kernel_timing_events_are_recorded_once():
     fa.fa_bwd(q, k, v, o, do, lse)            # the setting was used once: these events stay as they were
     torch.cuda.synchronize()
     assert e0.elapsed_time(e1) == main_ms
+    # A call that fails its checks takes the request too, so the next valid call records nothing.
+    fa.fa_debug_time_bwd_main(e0, e1)
+    lib = fa.load_library()
+    null9 = [None] * 9
+    assert lib.fa_bwd(*null9, B, H, N, d, 0.1, None, 0, None) == fa.FA_ERR_INVALID_ARG
+    fa.fa_bwd(q, k, v, o, do, lse)
+    torch.cuda.synchronize()
+    assert e0.elapsed_time(e1) == main_ms
     fa.fa_check_status()
