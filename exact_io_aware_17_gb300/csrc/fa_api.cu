@@ -130,8 +130,8 @@ cudaError_t set_max_dynamic_smem(const void* func, int bytes) {
 }
 
 cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int d, int N, int64_t heads, int box_cols,
-                             int box_rows) {
-    const TmapKey key{base, heads, d, N, box_cols, box_rows, 1};
+                             int box_rows, bool swizzle128) {
+    const TmapKey key{base, heads, d, N, box_cols, box_rows, swizzle128 ? 2 : 1};
     if (tmap_lookup(key, map)) return cudaSuccess;
     PFN_cuTensorMapEncodeTiled_v12000 encode;
     cudaError_t e = tmap_encoder(&encode);
@@ -141,7 +141,9 @@ cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int d, int N, 
     cuuint32_t box[3] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box, estr,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     tmap_store(key, *map);

@@ -106,23 +106,27 @@ struct BwdCfg {
     static constexpr uint32_t kKBytes = BK * D * 2;
     static constexpr uint32_t kQBytes = BQ * D * 2;
     static constexpr uint32_t kDSChunk = BK * 128;         // dS^T of one half: 128 key rows x 64 queries
-    static constexpr uint32_t kHalfDQBytes = HQ * D * 4;   // fp32 dQ rows [HQ][D] of one half
+    // d = 64 forms dQ = dS K with the step's queries as tensor-memory lanes (N = 64, no padding); the two
+    // warpgroups then split its 64 columns, and each stages [128 queries][32 columns].  d = 128 forms
+    // dQ^T = K^T dS^T (thread = head-dimension index) and the warpgroups split the queries.
+    static constexpr bool kRowDQ = D == 64;
+    static constexpr uint32_t kHalfDQBytes = HQ * D * 4;   // fp32 dQ of one warpgroup (16 or 32 KB)
     static constexpr uint32_t kSlotBytes = 2 * kDSChunk;   // holds a dO tile, dS^T or a half's dQ rows
     static constexpr uint32_t kOffK = 0;
-    static constexpr uint32_t kOffZero = kOffK + kKBytes;   // d = 64: zero half that pads K^T to M = 128
-    static constexpr uint32_t kZeroBytes = (D == 64) ? kChunkK : 0;
-    static constexpr uint32_t kOffV = kOffZero + kZeroBytes;
+    static constexpr uint32_t kOffV = kOffK + kKBytes;
     static constexpr uint32_t kOffQ = kOffV + kKBytes;
     static constexpr uint32_t kOffSlot = kOffQ + 2 * kQBytes;
     static constexpr uint32_t kOffStageB = kOffSlot + 2 * kSlotBytes;   // the second half's dQ rows
-    // The first half's rows are staged in the slot as stripes of 32 head-dimension columns ([HQ][32] fp32,
-    // one per warp), each added into the accumulator by a tensor reduce as soon as its warp has written it.
-    static constexpr int kStripes = D / 32;
+    // The first warpgroup's dQ is staged in the slot as stripes of 32 head-dimension columns, each added into
+    // the accumulator by a tensor reduce as soon as it is complete: at d = 128 one [HQ][32] stripe per warp
+    // (unswizzled), at d = 64 the warpgroup's whole [BQ][32] block (128-byte swizzled, written by 16-byte
+    // stores).
+    static constexpr int kStripes = kRowDQ ? 1 : D / 32;
     // d = 64: dS ready for dK (tensor memory) is signalled before the shared-memory copy for dQ^T, which
     // waits for dV to have read the slot; a barrier of its own covers that copy.  At d = 128 one signal
     // after both measured as fast (and 0.7 % faster at N = 32768).
     static constexpr bool kEarlyDsReady = D == 64;
-    static constexpr uint32_t kStripeBytes = HQ * 32 * 4;
+    static constexpr uint32_t kStripeBytes = (kRowDQ ? BQ : HQ) * 32 * 4;
     static constexpr uint32_t kRowBytes = BQ * 4;          // LSE2 or -D of one query block
     static constexpr uint32_t kOffRows = kOffStageB + kHalfDQBytes;    // [q stage][LSE2 | -D][BQ] floats
     static constexpr uint32_t kOffBar = kOffRows + 2 * 2 * kRowBytes;
@@ -132,11 +136,11 @@ struct BwdCfg {
     static constexpr uint32_t kAlignSlack = kSmemNeed + 1024 <= 232448 ? 1024 : 232448 - kSmemNeed;
     static constexpr uint32_t kSmemBytes = kSmemNeed + kAlignSlack;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-    // dQ^T reuses the columns of dP^T at d = 128 (all 512 are taken); at d = 64 it has 128 spare columns
-    // of its own, so the next dP^T need not wait for it to be moved out.
+    // dQ^T reuses the columns of dP^T at d = 128 (all 512 are taken); at d = 64 dQ has spare columns of its
+    // own, so the next dP^T need not wait for it to be moved out.
     static constexpr bool kOwnDQ = D == 64;
     static constexpr uint32_t kColDQ = kOwnDQ ? 256 + 2 * D : kColDP;
-    static_assert(kColDQ + 128 <= 512, "tensor memory columns");
+    static_assert(kColDQ + (kRowDQ ? D : 128) <= 512, "tensor memory columns");
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kQBytes <= kSlotBytes && kHalfDQBytes <= kSlotBytes, "slot contents");
     static_assert(kStripes * kStripeBytes == kHalfDQBytes && kStripes <= 4, "stripes of the first half");
@@ -172,7 +176,8 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         const int q0 = qblock(j, rot, Tq) * BQ;
         for (int w = 0; w < C::kStripes; ++w) {
             if (!mbar_wait(&bars->staged_a[t][w], (j >> 1) & 1, wc)) return false;
-            tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kStripeBytes, 32 * w, q0, head);
+            tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kStripeBytes,
+                              C::kRowDQ ? 0 : 32 * w, q0, head);
             if ((w + 1) % (C::kStripes / C::kChunks) == 0) bulk_commit_group();
         }
         return true;
@@ -229,7 +234,9 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
     WaitCtl* wc = &bars->wait;
     constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, 0, 0);   // S^T, dP^T: A and B K-major over the head dimension
     constexpr uint32_t idG = idesc_bf16_f32(BK, D, 0, 1);    // dV, dK: A from TMEM, B MN-major [q][d]
-    constexpr uint32_t idQ = idesc_bf16_f32(128, BQ, 1, 1);  // dQ^T: A = K^T (MN-major), B = dS^T (MN-major)
+    // dQ^T: A = K^T (MN-major), B = dS^T (MN-major).  d = 64, dQ: A = dS read MN-major from the slot's dS^T,
+    // B = K (MN-major over d).
+    constexpr uint32_t idQ = C::kRowDQ ? idesc_bf16_f32(BQ, D, 1, 1) : idesc_bf16_f32(128, BQ, 1, 1);
     // Operand descriptors are built once; each use only adds a constant byte offset.  K-major views
     // serve S^T and dP^T; MN-major views of the same tiles serve dV, dK and dQ^T.
     const uint64_t kK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
@@ -257,13 +264,16 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
             mma_ts(d, a + kk * 8, sdesc_advance(b0, (half * (HQ / 16) + kk) * 16 * 128), idG,
                    (acc || kk > 0) ? 1u : 0u);
     };
-    // dQ^T = K^T dS^T over the 128 keys, into the columns of dP^T (free once dK used dS^T) or, at d = 64,
-    // into columns of its own.
-    auto dq = [&](uint64_t b0) {
+    // dQ^T = K^T dS^T over the 128 keys, into the columns of dP^T (free once dK used dS^T); at d = 64
+    // dQ = dS K into columns of its own.
+    auto dq = [&](uint64_t ds0) {
         const uint32_t d = tmem + C::kColDQ;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk)
-            mma_ss(d, sdesc_advance(mK, kk * 16 * 128), sdesc_advance(b0, kk * 16 * 128), idQ, kk > 0);
+        for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t k = sdesc_advance(mK, kk * 16 * 128), ds = sdesc_advance(ds0, kk * 16 * 128);
+            if constexpr (C::kRowDQ) mma_ss(d, ds, k, idQ, kk > 0);
+            else mma_ss(d, k, ds, idQ, kk > 0);
+        }
     };
 
     // dP^T = V dO^T for the dO tile in `slot`, one 64-column chunk of the head dimension (four k-steps) at
@@ -347,8 +357,8 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
 // Order of step i: dS(i), P(i+1), then dQ(i) out of tensor memory (P(0) comes first).
 template <int D>
 __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, float* __restrict__ dq_acc,
-                             __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, int head, int k0, int N,
-                             int Tq, int rot, float scale, float scale_log2) {
+                             const CUtensorMap* tm_dq, __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv,
+                             int head, int k0, int N, int Tq, int rot, float scale, float scale_log2) {
     using C = BwdCfg<D>;
     WaitCtl* wc = &bars->wait;
     const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -442,6 +452,38 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
 
         if (i + 1 < Tq && !(ok = form_p(i + 1))) break;
 
+        if constexpr (C::kRowDQ) {
+            // dQ_i (d = 64): thread = query row r of the step, this warpgroup's 32 columns, staged as row r of
+            // a [BQ][32] fp32 block with 16-byte stores, 16-byte chunks XOR-swizzled by r % 8 (the tensor
+            // map's 128-byte swizzle): the first warpgroup's in the step's slot (dQ has read its dS^T), the
+            // second's in its own buffer once the previous step's reduce has read it.
+            if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
+            tc_fence_after();
+            uint32_t x[32];
+            tmem_ld32(tmem + lane_off + C::kColDQ + 32 * half, x);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bars->dq_empty);
+            if (half == 1 && i > 0) {
+                if (leader) {
+                    bulk_wait_group_read<0>();
+                    mbar_arrive(&bars->stage_b_free);
+                }
+                if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
+            }
+            uint8_t* rowp = smem + (half == 0 ? C::kOffSlot + s * C::kSlotBytes : C::kOffStageB) + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+            fence_proxy_async_smem();
+            mbar_arrive(half == 0 ? &bars->staged_a[s][0] : &bars->staged_b);
+            if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
+                tma_reduce_add_3d(tm_dq, smem + C::kOffStageB, 32, qblock(i, rot, Tq) * BQ, head);
+                bulk_commit_group();
+            }
+            continue;
+        }
         // dQ_i^T: this half's 64 query columns, thread = head-dimension index r.
         if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
         tc_fence_after();
@@ -554,7 +596,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&bars->do_full[t][0], 1);
             mbar_init(&bars->do_full[t][1], 1);
             mbar_init(&bars->dv_done[t], 1);
-            for (int w = 0; w < 4; ++w) mbar_init(&bars->staged_a[t][w], 32);
+            for (int w = 0; w < 4; ++w) mbar_init(&bars->staged_a[t][w], C::kRowDQ ? 128 : 32);
             mbar_init(&bars->p_ready[t], 128);
             mbar_init(&bars->ds_ready[t], 128);
         }
@@ -569,11 +611,6 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         mbar_init(&bars->mma_done, 1);
         bars->wait.abort = 0;
         fence_mbar_init();
-    }
-    if constexpr (C::kZeroBytes > 0) {
-        uint4* z = reinterpret_cast<uint4*>(smem + C::kOffZero);
-        for (uint32_t idx = threadIdx.x; idx < C::kZeroBytes / 16; idx += kThreads) z[idx] = make_uint4(0, 0, 0, 0);
-        fence_proxy_async_smem();
     }
     if (warp == kTmaWarp && lane == 0) {
         tma_prefetch_desc(&tm_q);
@@ -598,7 +635,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     } else if (warp == kMmaWarp) {
         if (lane == 0) bwd_mma<D>(smem, bars, tmem, Tq);
     } else {
-        bwd_softgrad<D>(smem, bars, tmem, dq_acc, dk, dv, head, k0, N, Tq, rot, scale, scale_log2);
+        bwd_softgrad<D>(smem, bars, tmem, dq_acc, &tm_dq, dk, dv, head, k0, N, Tq, rot, scale, scale_log2);
     }
 
     tc_fence_before();
@@ -703,7 +740,9 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     if ((e = make_tmap_bf16_3d(&tdo, dout, s.d, s.N, s.heads(), BQ)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tk, k, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
-    if ((e = make_tmap_f32_3d(&tdq, dq_acc, s.d, s.N, s.heads(), 32, HQ)) != cudaSuccess) return e;
+    // The dQ staging boxes: [HQ rows][32 columns] unswizzled (d = 128), [BQ rows][32 columns] swizzled (d = 64).
+    if ((e = make_tmap_f32_3d(&tdq, dq_acc, s.d, s.N, s.heads(), 32, C::kRowDQ ? BQ : HQ, C::kRowDQ)) != cudaSuccess)
+        return e;
     e = set_max_dynamic_smem((const void*)bwd_tc_kernel<D>, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
     const int bph = (s.N + BK - 1) / BK;

@@ -54,10 +54,11 @@ cudaError_t set_max_dynamic_smem(const void* func, int bytes);
 // `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.  Encoded maps are cached by
 // their arguments (address, shape, box), so repeated calls on the same buffers cost a table lookup.
 cudaError_t make_tmap_bf16_3d(CUtensorMap* map, const void* base, int d, int N, int64_t heads, int box_rows);
-// fp32 [heads][N][d] viewed as (d, N, heads), unswizzled boxes of box_cols x box_rows (box_cols * 4 bytes a
-// multiple of 16): the dQ accumulator as the target of tensor reduce-adds.
+// fp32 [heads][N][d] viewed as (d, N, heads), boxes of box_cols x box_rows (box_cols * 4 bytes a multiple of
+// 16; 128 bytes when swizzled): the dQ accumulator as the target of tensor reduce-adds.  swizzle128: the
+// shared-memory box has 128-byte swizzling (16-byte chunk c of row r at chunk c ^ (r % 8)).
 cudaError_t make_tmap_f32_3d(CUtensorMap* map, const float* base, int d, int N, int64_t heads, int box_cols,
-                             int box_rows);
+                             int box_rows, bool swizzle128);
 
 // Launchers (return cudaGetLastError() of their launches).
 cudaError_t launch_fwd_tc(const void* q, const void* k, const void* v, void* o, float* lse, const Shape& s,
