@@ -21,12 +21,12 @@
 //                         dK_j += dS^T Q_i              dS^T as bf16 from tensor memory
 //                         dQ_i^T = K_j^T dS^T           dS^T as bf16 from shared memory, into the
 //                                                       columns of dP^T (free once dK used dS^T)
-//                     and adds dQ_i into the fp32 accumulator with bulk reduce-add copies (the first
-//                     half's rows as one tensor reduce per 32-column stripe, the second half's as one
-//                     linear reduce).
+//                     and adds dQ_i into the fp32 accumulator with bulk reduce-add copies (at d = 128
+//                     the first half's rows as one tensor reduce per 32-column stripe, the second
+//                     half's as one linear reduce; d = 64 differs, see the end of this comment).
 //   bwd_dq_convert    dQ = bf16(scale * accumulator).
 //
-// Every product is 128 x 128 x 128 (M = 128 keys or head dimensions, N = 128 queries or head
+// At d = 128 every product is 128 x 128 x 128 (M = 128 keys or head dimensions, N = 128 queries or head
 // dimensions): N = 128 is the narrowest tcgen05 shape that runs at the full rate, which 64-query steps
 // (three of five products at N = 64) did not reach.  Tensor memory then holds exactly S^T, dP^T, dV and
 // dK (4 x 128 columns at d = 128), with dQ^T reusing the columns of dP^T.  The MMAs of step i run in the
@@ -48,8 +48,13 @@
 // second half's dQ rows have a buffer of their own.  The kernel has no static shared memory, so its
 // dynamic region starts aligned and needs no slack.
 //
-// For d = 64 the dQ^T product still uses M = 128: the A operand's second 64-row half points at a
-// zeroed shared-memory block, and the rows it produces are ignored.
+// d = 64 forms dQ_i = dS K_j instead (M = 128 queries as tensor-memory lanes, N = 64, into 64 columns of
+// its own): the A operand is the slot's dS^T read MN-major, so nothing is padded.  Each warpgroup then
+// moves 32 of the 64 columns out (thread = query row) and stages them as one [128][32] fp32 block,
+// 128-byte swizzled and written with 16-byte stores, which a single tensor reduce adds into the
+// accumulator: the first warpgroup's block in the step's slot, the second's in its own buffer.  (The same
+// layout at d = 128, two blocks per warpgroup, was measured correct and 0.6-1 % slower, so d = 128 keeps
+// the transposed product.)
 
 #include <cuda_bf16.h>
 #include <math.h>
@@ -121,7 +126,7 @@ struct BwdCfg {
     // the accumulator by a tensor reduce as soon as it is complete: at d = 128 one [HQ][32] stripe per warp
     // (unswizzled), at d = 64 the warpgroup's whole [BQ][32] block (128-byte swizzled, written by 16-byte
     // stores).
-    static constexpr int kStripes = kRowDQ ? 1 : D / 32;
+    static constexpr int kStripes = kRowDQ ? D / 64 : D / 32;
     // d = 64: dS ready for dK (tensor memory) is signalled before the shared-memory copy for dQ^T, which
     // waits for dV to have read the slot; a barrier of its own covers that copy.  At d = 128 one signal
     // after both measured as fast (and 0.7 % faster at N = 32768).
@@ -175,9 +180,9 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         const int t = j & 1;
         const int q0 = qblock(j, rot, Tq) * BQ;
         for (int w = 0; w < C::kStripes; ++w) {
-            if (!mbar_wait(&bars->staged_a[t][w], (j >> 1) & 1, wc)) return false;
-            tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kStripeBytes,
-                              C::kRowDQ ? 0 : 32 * w, q0, head);
+            // With the queries as rows every warp writes into every block, so one barrier covers them all.
+            if ((!C::kRowDQ || w == 0) && !mbar_wait(&bars->staged_a[t][w], (j >> 1) & 1, wc)) return false;
+            tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kStripeBytes, 32 * w, q0, head);
             if ((w + 1) % (C::kStripes / C::kChunks) == 0) bulk_commit_group();
         }
         return true;
@@ -367,7 +372,6 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool valid_key = k0 + r < N;
     const bool leader = (threadIdx.x % 128) == 0;
-    const bool dq_lane = r < D;                           // dQ^T rows >= D are the d = 64 padding
     const float* rows_base = reinterpret_cast<const float*>(smem + C::kOffRows);
     const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
 
@@ -459,8 +463,9 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
             // second's in its own buffer once the previous step's reduce has read it.
             if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
             tc_fence_after();
-            uint32_t x[32];
-            tmem_ld32(tmem + lane_off + C::kColDQ + 32 * half, x);
+            uint32_t x[D / 64][32];
+#pragma unroll
+            for (int b = 0; b < D / 64; ++b) tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * half + 32 * b, x[b]);
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&bars->dq_empty);
@@ -473,65 +478,64 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
             }
             uint8_t* rowp = smem + (half == 0 ? C::kOffSlot + s * C::kSlotBytes : C::kOffStageB) + r * 128;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4*>(rowp + ((j ^ (lane & 7)) << 4)) =
-                    make_uint4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+            for (int b = 0; b < D / 64; ++b)
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint4*>(rowp + b * C::kStripeBytes + ((j ^ (lane & 7)) << 4)) =
+                        make_uint4(x[b][4 * j], x[b][4 * j + 1], x[b][4 * j + 2], x[b][4 * j + 3]);
             fence_proxy_async_smem();
             mbar_arrive(half == 0 ? &bars->staged_a[s][0] : &bars->staged_b);
             if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
-                tma_reduce_add_3d(tm_dq, smem + C::kOffStageB, 32, qblock(i, rot, Tq) * BQ, head);
+                for (int b = 0; b < D / 64; ++b)
+                    tma_reduce_add_3d(tm_dq, smem + C::kOffStageB + b * C::kStripeBytes, D / 2 + 32 * b,
+                                      qblock(i, rot, Tq) * BQ, head);
                 bulk_commit_group();
             }
-            continue;
-        }
-        // dQ_i^T: this half's 64 query columns, thread = head-dimension index r.
-        if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
-        tc_fence_after();
-        // Every warp loads (lanes >= D hold the d = 64 padding rows, which are not staged).
-        uint32_t x[2][32];
-        tmem_ld32(tmem + lane_off + C::kColDQ + half * HQ, x[0]);
-        tmem_ld32(tmem + lane_off + C::kColDQ + half * HQ + 32, x[1]);
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(&bars->dq_empty);
-        // Stage the rows (fp32): the first half into the step's slot (dQ^T has read its dS^T) as this warp's
-        // stripe [HQ][32], the second half into its own buffer as rows [HQ][D].
-        // The second half's buffer is reused once the reduce of the previous step's rows has read it (it has
-        // had a whole step); only the thread that issued that reduce can wait for it.
-        if (half == 1 && i > 0) {
-            if (leader) {
-                bulk_wait_group_read<0>();
-                mbar_arrive(&bars->stage_b_free);
+        } else {
+            // dQ_i^T (d = 128): this half's 64 query columns, thread = head-dimension index r.
+            if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
+            tc_fence_after();
+            uint32_t x[2][32];
+            tmem_ld32(tmem + lane_off + C::kColDQ + half * HQ, x[0]);
+            tmem_ld32(tmem + lane_off + C::kColDQ + half * HQ + 32, x[1]);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(&bars->dq_empty);
+            // Stage the rows (fp32): the first half into the step's slot (dQ^T has read its dS^T) as this warp's
+            // stripe [HQ][32], the second half into its own buffer as rows [HQ][D].
+            // The second half's buffer is reused once the reduce of the previous step's rows has read it (it has
+            // had a whole step); only the thread that issued that reduce can wait for it.
+            if (half == 1 && i > 0) {
+                if (leader) {
+                    bulk_wait_group_read<0>();
+                    mbar_arrive(&bars->stage_b_free);
+                }
+                if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
             }
-            if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
-        }
-        if (half == 0) {
-            if (dq_lane) {
+            if (half == 0) {
                 float* stripe =
                     reinterpret_cast<float*>(smem + C::kOffSlot + s * C::kSlotBytes + quarter * C::kStripeBytes);
 #pragma unroll
                 for (int q = 0; q < HQ; ++q) stripe[q * 32 + lane] = __uint_as_float(x[q / 32][q % 32]);
                 fence_proxy_async_smem();
                 mbar_arrive(&bars->staged_a[s][quarter]);
-            }
-        } else {
-            float* stage = reinterpret_cast<float*>(smem + C::kOffStageB);
-            if (dq_lane) {
+            } else {
+                float* stage = reinterpret_cast<float*>(smem + C::kOffStageB);
 #pragma unroll
                 for (int q = 0; q < HQ; ++q) stage[q * D + r] = __uint_as_float(x[q / 32][q % 32]);
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->staged_b);
             }
-            fence_proxy_async_smem();
-            mbar_arrive(&bars->staged_b);
-        }
-        // The TMA thread reduces the first half; the second half's leader reduces its own.  A wait that
-        // gives up has set the abort flag, which stops the whole warp at its next wait.
-        if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
-            const int q0 = qblock(i, rot, Tq) * BQ + HQ;
-            const int rows = min(HQ, N - q0);
-            if (rows > 0) {
-                bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, smem + C::kOffStageB,
-                                    (uint32_t)(rows * D * 4));
-                bulk_commit_group();
+            // The TMA thread reduces the first half; the second half's leader reduces its own.  A wait that
+            // gives up has set the abort flag, which stops the whole warp at its next wait.
+            if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
+                const int q0 = qblock(i, rot, Tq) * BQ + HQ;
+                const int rows = min(HQ, N - q0);
+                if (rows > 0) {
+                    bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, smem + C::kOffStageB,
+                                        (uint32_t)(rows * D * 4));
+                    bulk_commit_group();
+                }
             }
         }
     }
