@@ -386,8 +386,7 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         tc_fence_after();
         const float* lse2 = rows_base + (j & 1) * 2 * BQ + half * HQ;
         uint32_t sr[2][32];
-        tmem_ld32(tmem + lane_off + C::kColS + half * HQ, sr[0]);
-        tmem_ld32(tmem + lane_off + C::kColS + half * HQ + 32, sr[1]);
+        tmem_ld64(tmem + lane_off + C::kColS + half * HQ, sr);
         tmem_ld_wait();
         uint32_t pk[32];
 #pragma unroll
@@ -420,8 +419,7 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         uint32_t pk[32];
         {
             uint32_t dr[2][32];
-            tmem_ld32(tmem + lane_off + C::kColDP + half * HQ, dr[0]);
-            tmem_ld32(tmem + lane_off + C::kColDP + half * HQ + 32, dr[1]);
+            tmem_ld64(tmem + lane_off + C::kColDP + half * HQ, dr);
             tmem_ld_wait();
 #pragma unroll
             for (int c = 0; c < HQ / 2; ++c) {
@@ -500,8 +498,7 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
             if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
             tc_fence_after();
             uint32_t x[2][32];
-            tmem_ld32(tmem + lane_off + C::kColDQ + half * HQ, x[0]);
-            tmem_ld32(tmem + lane_off + C::kColDQ + half * HQ + 32, x[1]);
+            tmem_ld64(tmem + lane_off + C::kColDQ + half * HQ, x);
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(&bars->dq_empty);

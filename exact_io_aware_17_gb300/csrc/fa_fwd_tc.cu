@@ -291,6 +291,7 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
         tc_fence_after();
         const uint32_t tS = C::kThreeS ? tmem + C::col_s3(2 * j + t) + lane_off : tS1;
         uint32_t r[4][32];
+        // Four 32-column loads: one 128-column load measured 0.3-2 % slower here (unlike the backward).
 #pragma unroll
         for (int q = 0; q < 4; ++q) tmem_ld32(tS + q * 32, r[q]);
         tmem_ld_wait();
