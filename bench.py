@@ -399,11 +399,11 @@ def _e2e(fa, w, inp_cpu, dev, steps):
 # stale: the JSON line then reports traffic null and says so.
 TRAFFIC = {
     ("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): {
-        "bytes": 203138048 + 83817984,
+        "bytes": 202488064 + 82951936,
         "profile": "profiles/dram_per_launch_bench_B1-H16-N8192-d128.md",
         "kernel": "bwd_tc_kernel<128>",
         "sources": ("exact_io_aware_17_gb300/csrc/fa_bwd_tc.cu", "exact_io_aware_17_gb300/csrc/fa_ptx.cuh"),
-        "sha256": "a0be7423f982d390cc026bf8b5a80e40db487433f64f7492bfd7a0463b5a4a66",
+        "sha256": "4ea1dbfbd52ad2787ce37f61f29b076a12e246286db8a55278ea7102b9b9ea78",
     },
 }
 

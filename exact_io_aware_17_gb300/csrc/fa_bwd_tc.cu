@@ -19,42 +19,37 @@
 //                         dS^T = P^T o (dP^T - D_i)
 //                         dV_j += P^T dO_i              P^T as bf16 from tensor memory
 //                         dK_j += dS^T Q_i              dS^T as bf16 from tensor memory
-//                         dQ_i^T = K_j^T dS^T           dS^T as bf16 from shared memory, into the
-//                                                       columns of dP^T (free once dK used dS^T)
-//                     and adds dQ_i into the fp32 accumulator with bulk reduce-add copies (at d = 128
-//                     the first half's rows as one tensor reduce per 32-column stripe, the second
-//                     half's as one linear reduce; d = 64 differs, see the end of this comment).
+//                         dQ_i = dS K_j                 dS as bf16 from shared memory (the slot's dS^T
+//                                                       read MN-major), queries as tensor-memory lanes
+//                     and adds dQ_i into the fp32 accumulator with tensor reduce-add copies.
 //   bwd_dq_convert    dQ = bf16(scale * accumulator).
 //
-// At d = 128 every product is 128 x 128 x 128 (M = 128 keys or head dimensions, N = 128 queries or head
+// At d = 128 every product is 128 x 128 x 128 (M = 128 keys or queries, N = 128 queries or head
 // dimensions): N = 128 is the narrowest tcgen05 shape that runs at the full rate, which 64-query steps
 // (three of five products at N = 64) did not reach.  Tensor memory then holds exactly S^T, dP^T, dV and
-// dK (4 x 128 columns at d = 128), with dQ^T reusing the columns of dP^T.  The MMAs of step i run in the
-// order dV(i), S^T(i+1), dK(i), dQ^T(i), dP^T(i+1): the next S^T goes right behind dV (its columns held
-// P^T, which dV has just read), so forming P(i+1) overlaps dK and dQ^T on the tensor core.
+// dK (4 x 128 columns at d = 128), with dQ reusing the columns of dP^T; at d = 64 dQ has 64 columns of its
+// own.  The MMAs of step i run in the order dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1): the next S^T goes
+// right behind dV (its columns held P^T, which dV has just read), so forming P(i+1) overlaps dK and dQ on
+// the tensor core.
 //
 // Warp roles (320 threads): warps 0-3 and 4-7 are two warpgroups that own the same 128 key rows
-// (tensor-memory lanes) and split each step's queries, 64 each: they form P^T and dS^T for their half,
-// then move their half of dQ_i^T out of tensor memory (thread = head-dimension index) and stage it, and
-// at the end write dV (warps 0-3) and dK (warps 4-7).  Warp 8 issues the TMA loads and the first half's
-// reduce-adds, warp 9 allocates tensor memory and issues the MMAs; the second half's reduce-adds come
-// from its own leader thread.
+// (tensor-memory lanes) and split each step's queries, 64 each, for P^T and dS^T; for dQ the lanes are
+// the step's 128 queries and the warpgroups split the head dimension, d / 2 columns each, which they move
+// out of tensor memory (thread = query row) and stage.  At the end warps 0-3 write dV and warps 4-7 dK.
+// Warp 8 issues the TMA loads and the first warpgroup's reduce-adds, warp 9 allocates tensor memory and
+// issues the MMAs; the second warpgroup's reduce-adds come from its own leader thread.
 //
 // Shared memory (d = 128: 226 KB): K and V resident, two Q stages, and two slots that each hold a step's dO
-// tile, then its dS^T (once dV has read dO), then the first half's fp32 dQ rows (once dQ^T has read dS^T),
-// one [64][32] stripe per warp; the TMA thread adds each stripe into the accumulator as soon as its warp
-// has written it and loads the dO tile of step i + 2 there by 64-column chunks, each once the stripes
-// under it have been read; the MMA thread starts dP^T(i+2) on the first chunk.  The
-// second half's dQ rows have a buffer of their own.  The kernel has no static shared memory, so its
-// dynamic region starts aligned and needs no slack.
+// tile, then its dS^T (once dV has read dO), then the first warpgroup's fp32 dQ columns (once dQ has read
+// dS^T) as d / 64 [128][32] blocks, 128-byte swizzled and written with 16-byte stores; the TMA thread adds
+// each block into the accumulator with one tensor reduce and loads the dO tile of step i + 2 there by
+// 64-column chunks, each once the block under it has been read; the MMA thread starts dP^T(i+2) on the
+// first chunk.  The second warpgroup's blocks have a buffer of their own.  The kernel has no static shared
+// memory, so its dynamic region starts aligned and needs no slack.
 //
-// d = 64 forms dQ_i = dS K_j instead (M = 128 queries as tensor-memory lanes, N = 64, into 64 columns of
-// its own): the A operand is the slot's dS^T read MN-major, so nothing is padded.  Each warpgroup then
-// moves 32 of the 64 columns out (thread = query row) and stages them as one [128][32] fp32 block,
-// 128-byte swizzled and written with 16-byte stores, which a single tensor reduce adds into the
-// accumulator: the first warpgroup's block in the step's slot, the second's in its own buffer.  (The same
-// layout at d = 128, two blocks per warpgroup, was measured correct and 0.6-1 % slower, so d = 128 keeps
-// the transposed product.)
+// (An earlier layout formed dQ^T = K^T dS^T at d = 128, thread = head-dimension index, each warp staging a
+// [64][32] stripe with scalar stores: once the tensor-memory loads were widened to 64 columns, the present
+// layout measured 0.6-0.7 % faster, and it serves both head sizes.)
 
 #include <cuda_bf16.h>
 #include <math.h>
@@ -82,12 +77,12 @@ struct BwdBarriers {
     uint64_t q_empty[2];           // dK of that step has read the Q tile
     uint64_t do_full[2][2];        // [slot][64-column chunk]: that chunk of a step's dO tile is in its slot
     uint64_t dv_done[2];           // dV of that step has read dO: the slot takes dS^T
-    uint64_t staged_a[2][4];       // one 32-column stripe of the first half's dQ rows is in the slot
+    uint64_t staged_a[2];          // the first warpgroup's dQ columns are staged in the slot
     uint64_t s_full;
     uint64_t dp_full;
     uint64_t p_ready;              // both halves' P^T of a step are in tensor memory (256 arrivals)
     uint64_t ds_ready[2];          // a half's dS^T is in tensor memory (d = 128: and in the step's slot)
-    uint64_t ds_smem;              // d = 64: both halves' dS^T are in the step's slot (what dQ^T reads)
+    uint64_t ds_smem;              // d = 64: both halves' dS^T are in the step's slot (what dQ reads)
     uint64_t dq_full;
     uint64_t dq_empty;
     uint64_t staged_b;             // the second half's dQ rows are in their staging buffer
@@ -99,10 +94,10 @@ struct BwdBarriers {
 };
 
 // Shared memory.  K and V stay resident; Q has two stages.  Each step's dO tile lives in one of two
-// slots, and the slot is reused within the step: once dV has read dO it takes the step's dS^T (the B
-// operand of dQ^T), and once dQ^T has read that it takes the first half's fp32 dQ rows, which the TMA
-// thread adds into the accumulator before loading the dO tile of step i + 2 there.  The second half's
-// dQ rows have a buffer of their own.
+// slots, and the slot is reused within the step: once dV has read dO it takes the step's dS^T (the A
+// operand of dQ), and once dQ has read that it takes the first warpgroup's fp32 dQ columns, which the
+// TMA thread adds into the accumulator before loading the dO tile of step i + 2 there.  The second
+// warpgroup's columns have a buffer of their own.
 template <int D>
 struct BwdCfg {
     static constexpr int kChunks = D / 64;
@@ -111,27 +106,23 @@ struct BwdCfg {
     static constexpr uint32_t kKBytes = BK * D * 2;
     static constexpr uint32_t kQBytes = BQ * D * 2;
     static constexpr uint32_t kDSChunk = BK * 128;         // dS^T of one half: 128 key rows x 64 queries
-    // d = 64 forms dQ = dS K with the step's queries as tensor-memory lanes (N = 64, no padding); the two
-    // warpgroups then split its 64 columns, and each stages [128 queries][32 columns].  d = 128 forms
-    // dQ^T = K^T dS^T (thread = head-dimension index) and the warpgroups split the queries.
-    static constexpr bool kRowDQ = D == 64;
-    static constexpr uint32_t kHalfDQBytes = HQ * D * 4;   // fp32 dQ of one warpgroup (16 or 32 KB)
+    // dQ = dS K is formed with the step's queries as tensor-memory lanes (M = 128, N = d); the two
+    // warpgroups split its d columns, and each stages [128 queries][d / 2] fp32.
+    static constexpr uint32_t kHalfDQBytes = BQ * (D / 2) * 4;   // fp32 dQ of one warpgroup (16 or 32 KB)
     static constexpr uint32_t kSlotBytes = 2 * kDSChunk;   // holds a dO tile, dS^T or a half's dQ rows
     static constexpr uint32_t kOffK = 0;
     static constexpr uint32_t kOffV = kOffK + kKBytes;
     static constexpr uint32_t kOffQ = kOffV + kKBytes;
     static constexpr uint32_t kOffSlot = kOffQ + 2 * kQBytes;
     static constexpr uint32_t kOffStageB = kOffSlot + 2 * kSlotBytes;   // the second half's dQ rows
-    // The first warpgroup's dQ is staged in the slot as stripes of 32 head-dimension columns, each added into
-    // the accumulator by a tensor reduce as soon as it is complete: at d = 128 one [HQ][32] stripe per warp
-    // (unswizzled), at d = 64 the warpgroup's whole [BQ][32] block (128-byte swizzled, written by 16-byte
-    // stores).
-    static constexpr int kStripes = kRowDQ ? D / 64 : D / 32;
-    // d = 64: dS ready for dK (tensor memory) is signalled before the shared-memory copy for dQ^T, which
+    // A warpgroup's dQ columns are staged as [BQ][32] fp32 blocks (128-byte swizzled, written by 16-byte
+    // stores), d / 64 of them, each added into the accumulator by one tensor reduce.
+    static constexpr int kStripes = D / 64;
+    // d = 64: dS ready for dK (tensor memory) is signalled before the shared-memory copy for dQ, which
     // waits for dV to have read the slot; a barrier of its own covers that copy.  At d = 128 one signal
     // after both measured as fast (and 0.7 % faster at N = 32768).
     static constexpr bool kEarlyDsReady = D == 64;
-    static constexpr uint32_t kStripeBytes = (kRowDQ ? BQ : HQ) * 32 * 4;
+    static constexpr uint32_t kStripeBytes = BQ * 32 * 4;
     static constexpr uint32_t kRowBytes = BQ * 4;          // LSE2 or -D of one query block
     static constexpr uint32_t kOffRows = kOffStageB + kHalfDQBytes;    // [q stage][LSE2 | -D][BQ] floats
     static constexpr uint32_t kOffBar = kOffRows + 2 * 2 * kRowBytes;
@@ -141,14 +132,14 @@ struct BwdCfg {
     static constexpr uint32_t kAlignSlack = kSmemNeed + 1024 <= 232448 ? 1024 : 232448 - kSmemNeed;
     static constexpr uint32_t kSmemBytes = kSmemNeed + kAlignSlack;
     static constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 256 + D;
-    // dQ^T reuses the columns of dP^T at d = 128 (all 512 are taken); at d = 64 dQ has spare columns of its
+    // dQ reuses the columns of dP^T at d = 128 (all 512 are taken); at d = 64 it has spare columns of its
     // own, so the next dP^T need not wait for it to be moved out.
     static constexpr bool kOwnDQ = D == 64;
     static constexpr uint32_t kColDQ = kOwnDQ ? 256 + 2 * D : kColDP;
-    static_assert(kColDQ + (kRowDQ ? D : 128) <= 512, "tensor memory columns");
+    static_assert(kColDQ + D <= 512, "tensor memory columns");
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kQBytes <= kSlotBytes && kHalfDQBytes <= kSlotBytes, "slot contents");
-    static_assert(kStripes * kStripeBytes == kHalfDQBytes && kStripes <= 4, "stripes of the first half");
+    static_assert(kStripes * kStripeBytes == kHalfDQBytes && kStripes == kChunks, "one block per dO chunk");
     static_assert(kSmemNeed <= 232448, "shared memory per CTA");
 };
 
@@ -171,19 +162,18 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         tma_load_3d(smem + C::kOffK + c * C::kChunkK, tm_k, &bars->kv_full, c * 64, k0, head, pol_keep);
         tma_load_3d(smem + C::kOffV + c * C::kChunkK, tm_v, &bars->kv_full, c * 64, k0, head, pol_keep);
     }
-    // The first half's dQ rows of step j end up in slot j % 2, one stripe per warp.  This thread adds each
-    // stripe into the accumulator as soon as it is there (rows past N are clipped by the tensor map) and
-    // reloads the slot once the reduces have read it, so it owns the slot's whole cycle.
-    // One bulk group per 64-column chunk of the dO tile that reloads the slot (the stripes under chunk c),
-    // so that chunk c can load as soon as its group has been read.
+    // The first warpgroup's dQ columns of step j end up in slot j % 2 as d / 64 [BQ][32] blocks.  This
+    // thread adds each block into the accumulator once the warpgroup has staged them (rows past N are
+    // clipped by the tensor map) and reloads the slot once the reduces have read it, so it owns the slot's
+    // whole cycle.  Block c lies under chunk c of the dO tile that reloads the slot and is its own bulk
+    // group, so that chunk c can load as soon as that block has been read.
     auto reduce_first_half = [&](int j) -> bool {
         const int t = j & 1;
         const int q0 = qblock(j, rot, Tq) * BQ;
+        if (!mbar_wait(&bars->staged_a[t], (j >> 1) & 1, wc)) return false;
         for (int w = 0; w < C::kStripes; ++w) {
-            // With the queries as rows every warp writes into every block, so one barrier covers them all.
-            if ((!C::kRowDQ || w == 0) && !mbar_wait(&bars->staged_a[t][w], (j >> 1) & 1, wc)) return false;
             tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kStripeBytes, 32 * w, q0, head);
-            if ((w + 1) % (C::kStripes / C::kChunks) == 0) bulk_commit_group();
+            bulk_commit_group();
         }
         return true;
     };
@@ -210,7 +200,7 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
 
         if (i >= 2 && !(ok = reduce_first_half(i - 2))) break;
         for (int c = 0; c < C::kChunks; ++c) {
-            // Chunk c overwrites the stripes of reduce group c (the groups are read in order).
+            // Chunk c overwrites the block of reduce group c (the groups are read in order).
             if (i >= 2) {
                 if (C::kChunks == 2 && c == 0) bulk_wait_group_read<1>();
                 else bulk_wait_group_read<0>();
@@ -230,20 +220,19 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         for (int c = 0; c < C::kChunks; ++c) drain_wait(&bars->do_full[i & 1][c], (i >> 1) & 1, wc);
 }
 
-// MMA order of step i: dV(i), S^T(i+1), dK(i), dQ^T(i), dP^T(i+1).  S^T of the next step goes right
+// MMA order of step i: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1).  S^T of the next step goes right
 // behind dV (its columns held P^T, which dV has just read), so the softmax warps can form P(i+1) while
-// the tensor core works on dK and dQ^T; dP^T(i+1) waits until dQ^T(i) has left its columns.
+// the tensor core works on dK and dQ; at d = 128 dP^T(i+1) waits until dQ(i) has left its columns.
 template <int D>
 __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq) {
     using C = BwdCfg<D>;
     WaitCtl* wc = &bars->wait;
     constexpr uint32_t idS = idesc_bf16_f32(BK, BQ, 0, 0);   // S^T, dP^T: A and B K-major over the head dimension
     constexpr uint32_t idG = idesc_bf16_f32(BK, D, 0, 1);    // dV, dK: A from TMEM, B MN-major [q][d]
-    // dQ^T: A = K^T (MN-major), B = dS^T (MN-major).  d = 64, dQ: A = dS read MN-major from the slot's dS^T,
-    // B = K (MN-major over d).
-    constexpr uint32_t idQ = C::kRowDQ ? idesc_bf16_f32(BQ, D, 1, 1) : idesc_bf16_f32(128, BQ, 1, 1);
+    // dQ: A = dS read MN-major from the slot's dS^T, B = K (MN-major over d).
+    constexpr uint32_t idQ = idesc_bf16_f32(BQ, D, 1, 1);
     // Operand descriptors are built once; each use only adds a constant byte offset.  K-major views
-    // serve S^T and dP^T; MN-major views of the same tiles serve dV, dK and dQ^T.
+    // serve S^T and dP^T; MN-major views of the same tiles serve dV, dK and dQ.
     const uint64_t kK = sdesc_sw128(smem_u32(smem + C::kOffK), 16, 1024);
     const uint64_t kV = sdesc_sw128(smem_u32(smem + C::kOffV), 16, 1024);
     const uint64_t kQ = sdesc_sw128(smem_u32(smem + C::kOffQ), 16, 1024);
@@ -269,16 +258,13 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
             mma_ts(d, a + kk * 8, sdesc_advance(b0, (half * (HQ / 16) + kk) * 16 * 128), idG,
                    (acc || kk > 0) ? 1u : 0u);
     };
-    // dQ^T = K^T dS^T over the 128 keys, into the columns of dP^T (free once dK used dS^T); at d = 64
-    // dQ = dS K into columns of its own.
+    // dQ = dS K over the 128 keys: at d = 128 into the columns of dP^T (free once dK used dS^T), at d = 64
+    // into columns of its own.
     auto dq = [&](uint64_t ds0) {
         const uint32_t d = tmem + C::kColDQ;
 #pragma unroll
-        for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t k = sdesc_advance(mK, kk * 16 * 128), ds = sdesc_advance(ds0, kk * 16 * 128);
-            if constexpr (C::kRowDQ) mma_ss(d, ds, k, idQ, kk > 0);
-            else mma_ss(d, k, ds, idQ, kk > 0);
-        }
+        for (int kk = 0; kk < BK / 16; ++kk)
+            mma_ss(d, sdesc_advance(ds0, kk * 16 * 128), sdesc_advance(mK, kk * 16 * 128), idQ, kk > 0);
     };
 
     // dP^T = V dO^T for the dO tile in `slot`, one 64-column chunk of the head dimension (four k-steps) at
@@ -334,7 +320,7 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         }
         if (!ok) break;
         mma_commit(&bars->q_empty[s]);
-        // dQ^T reads both halves' dS^T from the slot (at d = 128 ds_ready already covered it).
+        // dQ reads both halves' dS^T from the slot (at d = 128 ds_ready already covered it).
         if constexpr (C::kEarlyDsReady) {
             if (!(ok = mbar_wait_poll(&bars->ds_smem, i & 1, wc))) break;
             tc_fence_after();
@@ -347,7 +333,7 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         mma_commit(&bars->dq_full);
         if (i + 1 < Tq) {
             if (!(ok = mbar_wait_poll(&bars->do_full[s1][0], ((i + 1) >> 1) & 1, wc))) break;
-            // At d = 128 the columns of dP^T hold dQ^T of step i until it has been moved out.
+            // At d = 128 the columns of dP^T hold dQ of step i until it has been moved out.
             if (!C::kOwnDQ && !(ok = mbar_wait_poll(&bars->dq_empty, i & 1, wc))) break;
             tc_fence_after();
             if (!(ok = dp_by_chunks(s1, ((i + 1) >> 1) & 1))) break;
@@ -359,8 +345,9 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
     drain_wait(&bars->mma_done, 0, wc);
 }
 
-// Warps 0-7.  Thread = key row r of the CTA (tensor-memory lane) in the softmax-gradient part and
-// head-dimension index r in the dQ part; `half` selects queries [64 half, 64 half + 64) of each step.
+// Warps 0-7.  Thread = key row r of the CTA (tensor-memory lane) in the softmax-gradient part, where
+// `half` selects queries [64 half, 64 half + 64) of each step, and query row r of the step in the dQ
+// part, where `half` selects head-dimension columns [d/2 half, d/2 half + d/2).
 // Order of step i: dS(i), P(i+1), then dQ(i) out of tensor memory (P(0) comes first).
 template <int D>
 __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, float* __restrict__ dq_acc,
@@ -440,7 +427,7 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
             mbar_arrive(&bars->ds_ready[half]);
         }
         // dS^T row r into this half's chunk of the step's slot (128-byte rows, 16-byte chunks XOR-swizzled
-        // by r % 8) for dQ^T, once dV has read the dO tile there.
+        // by r % 8) for dQ, once dV has read the dO tile there.
         if (!(ok = warp_wait(&bars->dv_done[s], (i >> 1) & 1, wc))) break;
         uint8_t* row = smem + C::kOffSlot + s * C::kSlotBytes + half * C::kDSChunk + r * 128;
 #pragma unroll
@@ -458,86 +445,39 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
 
         if (i + 1 < Tq && !(ok = form_p(i + 1))) break;
 
-        if constexpr (C::kRowDQ) {
-            // dQ_i (d = 64): thread = query row r of the step, this warpgroup's 32 columns, staged as row r of
-            // a [BQ][32] fp32 block with 16-byte stores, 16-byte chunks XOR-swizzled by r % 8 (the tensor
-            // map's 128-byte swizzle): the first warpgroup's in the step's slot (dQ has read its dS^T), the
-            // second's in its own buffer once the previous step's reduce has read it.
-            if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
-            tc_fence_after();
-            uint32_t x[D / 64][32];
-#pragma unroll
-            for (int b = 0; b < D / 64; ++b) tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * half + 32 * b, x[b]);
-            tmem_ld_wait();
-            tc_fence_before();
-            if constexpr (!C::kOwnDQ) mbar_arrive(&bars->dq_empty);
-            if (half == 1 && i > 0) {
-                if (leader) {
-                    bulk_wait_group_read<0>();
-                    mbar_arrive(&bars->stage_b_free);
-                }
-                if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
+        // dQ_i: thread = query row r of the step, this warpgroup's d / 2 columns, staged as row r of d / 64
+        // [BQ][32] fp32 blocks with 16-byte stores, 16-byte chunks XOR-swizzled by r % 8 (the tensor map's
+        // 128-byte swizzle): the first warpgroup's in the step's slot (dQ has read its dS^T), the second's in
+        // its own buffer once the previous step's reduce has read it.
+        if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
+        tc_fence_after();
+        uint32_t x[D / 64][32];
+        if constexpr (D == 128) tmem_ld64(tmem + lane_off + C::kColDQ + (D / 2) * half, x);
+        else tmem_ld32(tmem + lane_off + C::kColDQ + (D / 2) * half, x[0]);
+        tmem_ld_wait();
+        tc_fence_before();
+        if constexpr (!C::kOwnDQ) mbar_arrive(&bars->dq_empty);
+        if (half == 1 && i > 0) {
+            if (leader) {
+                bulk_wait_group_read<0>();
+                mbar_arrive(&bars->stage_b_free);
             }
-            uint8_t* rowp = smem + (half == 0 ? C::kOffSlot + s * C::kSlotBytes : C::kOffStageB) + r * 128;
+            if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
+        }
+        uint8_t* rowp = smem + (half == 0 ? C::kOffSlot + s * C::kSlotBytes : C::kOffStageB) + r * 128;
 #pragma unroll
+        for (int b = 0; b < D / 64; ++b)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(rowp + b * C::kStripeBytes + ((j ^ (lane & 7)) << 4)) =
+                    make_uint4(x[b][4 * j], x[b][4 * j + 1], x[b][4 * j + 2], x[b][4 * j + 3]);
+        fence_proxy_async_smem();
+        mbar_arrive(half == 0 ? &bars->staged_a[s] : &bars->staged_b);
+        if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
             for (int b = 0; b < D / 64; ++b)
-#pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<uint4*>(rowp + b * C::kStripeBytes + ((j ^ (lane & 7)) << 4)) =
-                        make_uint4(x[b][4 * j], x[b][4 * j + 1], x[b][4 * j + 2], x[b][4 * j + 3]);
-            fence_proxy_async_smem();
-            mbar_arrive(half == 0 ? &bars->staged_a[s][0] : &bars->staged_b);
-            if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
-                for (int b = 0; b < D / 64; ++b)
-                    tma_reduce_add_3d(tm_dq, smem + C::kOffStageB + b * C::kStripeBytes, D / 2 + 32 * b,
-                                      qblock(i, rot, Tq) * BQ, head);
-                bulk_commit_group();
-            }
-        } else {
-            // dQ_i^T (d = 128): this half's 64 query columns, thread = head-dimension index r.
-            if (!(ok = warp_wait(&bars->dq_full, i & 1, wc))) break;
-            tc_fence_after();
-            uint32_t x[2][32];
-            tmem_ld64(tmem + lane_off + C::kColDQ + half * HQ, x);
-            tmem_ld_wait();
-            tc_fence_before();
-            mbar_arrive(&bars->dq_empty);
-            // Stage the rows (fp32): the first half into the step's slot (dQ^T has read its dS^T) as this warp's
-            // stripe [HQ][32], the second half into its own buffer as rows [HQ][D].
-            // The second half's buffer is reused once the reduce of the previous step's rows has read it (it has
-            // had a whole step); only the thread that issued that reduce can wait for it.
-            if (half == 1 && i > 0) {
-                if (leader) {
-                    bulk_wait_group_read<0>();
-                    mbar_arrive(&bars->stage_b_free);
-                }
-                if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
-            }
-            if (half == 0) {
-                float* stripe =
-                    reinterpret_cast<float*>(smem + C::kOffSlot + s * C::kSlotBytes + quarter * C::kStripeBytes);
-#pragma unroll
-                for (int q = 0; q < HQ; ++q) stripe[q * 32 + lane] = __uint_as_float(x[q / 32][q % 32]);
-                fence_proxy_async_smem();
-                mbar_arrive(&bars->staged_a[s][quarter]);
-            } else {
-                float* stage = reinterpret_cast<float*>(smem + C::kOffStageB);
-#pragma unroll
-                for (int q = 0; q < HQ; ++q) stage[q * D + r] = __uint_as_float(x[q / 32][q % 32]);
-                fence_proxy_async_smem();
-                mbar_arrive(&bars->staged_b);
-            }
-            // The TMA thread reduces the first half; the second half's leader reduces its own.  A wait that
-            // gives up has set the abort flag, which stops the whole warp at its next wait.
-            if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
-                const int q0 = qblock(i, rot, Tq) * BQ + HQ;
-                const int rows = min(HQ, N - q0);
-                if (rows > 0) {
-                    bulk_reduce_add_f32(dq_acc + ((size_t)head * N + (size_t)q0) * D, smem + C::kOffStageB,
-                                        (uint32_t)(rows * D * 4));
-                    bulk_commit_group();
-                }
-            }
+                tma_reduce_add_3d(tm_dq, smem + C::kOffStageB + b * C::kStripeBytes, D / 2 + 32 * b,
+                                  qblock(i, rot, Tq) * BQ, head);
+            bulk_commit_group();
         }
     }
     if (leader) bulk_wait_group<0>();
@@ -601,7 +541,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             mbar_init(&bars->do_full[t][0], 1);
             mbar_init(&bars->do_full[t][1], 1);
             mbar_init(&bars->dv_done[t], 1);
-            for (int w = 0; w < 4; ++w) mbar_init(&bars->staged_a[t][w], C::kRowDQ ? 128 : 32);
+            mbar_init(&bars->staged_a[t], 128);
             mbar_init(&bars->ds_ready[t], 128);
         }
         mbar_init(&bars->staged_b, 128);
@@ -746,7 +686,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     if ((e = make_tmap_bf16_3d(&tk, k, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
     // The dQ staging boxes: [HQ rows][32 columns] unswizzled (d = 128), [BQ rows][32 columns] swizzled (d = 64).
-    if ((e = make_tmap_f32_3d(&tdq, dq_acc, s.d, s.N, s.heads(), 32, C::kRowDQ ? BQ : HQ, C::kRowDQ)) != cudaSuccess)
+    if ((e = make_tmap_f32_3d(&tdq, dq_acc, s.d, s.N, s.heads(), 32, BQ, true)) != cudaSuccess)
         return e;
     e = set_max_dynamic_smem((const void*)bwd_tc_kernel<D>, (int)C::kSmemBytes);
     if (e != cudaSuccess) return e;
