@@ -363,55 +363,68 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
             tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&bars->p_full[t][j & 1]);
-            continue;
-        }
-        const float m_new = fmaxf(m_run, mx * scale_log2);
-        const bool rescale = m_new - m_run > kRescaleThreshold;  // always true for the first block
-        float alpha = 1.f;
-        if (rescale) {
-            alpha = ex2(m_run - m_new);
-            m_run = m_new;
-        }
-        const float neg_m = -m_run;
-        // s * scale*log2e - m and the row sum run on packed pairs (f32x2): two results per instruction.
-        const uint64_t sl2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(neg_m, neg_m);
-        uint64_t s2[4] = {0, 0, 0, 0};
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t pk[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                const int q = 2 * h + c / 16, e = (2 * c) % 32;
-                const uint64_t x2 = ffma2(f2_pack(__uint_as_float(r[q][e]), __uint_as_float(r[q][e + 1])), sl2, nm2);
-                float x0, x1;
-                f2_unpack(x2, x0, x1);
-                const float p0 = ex2(x0), p1 = ex2(x1);
-                s2[c % 4] = fadd2(s2[c % 4], f2_pack(p0, p1));
-                pk[c] = pack_bf16(p0, p1);
+        } else {
+            const float m_new = fmaxf(m_run, mx * scale_log2);
+            const bool rescale = m_new - m_run > kRescaleThreshold;  // always true for the first block
+            float alpha = 1.f;
+            if (rescale) {
+                alpha = ex2(m_run - m_new);
+                m_run = m_new;
             }
-            tmem_st32(tS + h * 32, pk);
-        }
-        float sc[8];
+            const float neg_m = -m_run;
+            // s * scale*log2e - m and the row sum run on packed pairs (f32x2): two results per instruction.
+            const uint64_t sl2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(neg_m, neg_m);
+            uint64_t s2[4] = {0, 0, 0, 0};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) f2_unpack(s2[k], sc[2 * k], sc[2 * k + 1]);
-        const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
-        l_run = l_run * alpha + sum;
-        if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-            // With three S buffers, PV of the previous block may still be accumulating into O.
-            if (C::kThreeS && !(ok = prev_pv_done<D>(bars, t, j, T, wc))) break;
+            // P of keys [64 h, 64 h + 64) as 32 bf16 pairs.
+            auto exp_half = [&](int h, uint32_t (&pk)[32]) {
 #pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t x[32];
-                tmem_ld32(tO + q * 32, x);
-                tmem_ld_wait();
+                for (int c = 0; c < 32; ++c) {
+                    const int q = 2 * h + c / 16, e = (2 * c) % 32;
+                    const uint64_t x2 = ffma2(f2_pack(__uint_as_float(r[q][e]), __uint_as_float(r[q][e + 1])), sl2, nm2);
+                    float x0, x1;
+                    f2_unpack(x2, x0, x1);
+                    const float p0 = ex2(x0), p1 = ex2(x1);
+                    s2[c % 4] = fadd2(s2[c % 4], f2_pack(p0, p1));
+                    pk[c] = pack_bf16(p0, p1);
+                }
+            };
+            if constexpr (D == 128) {
+                // One 64-column store: 0.5-0.8 % faster here, 0.7 % slower at d = 64 (measured).
+                uint32_t pk[2][32];
+                exp_half(0, pk[0]);
+                exp_half(1, pk[1]);
+                tmem_st64(tS, pk);
+            } else {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * alpha);
-                tmem_st32(tO + q * 32, x);
+                for (int h = 0; h < 2; ++h) {
+                    uint32_t pk[32];
+                    exp_half(h, pk);
+                    tmem_st32(tS + h * 32, pk);
+                }
             }
+            float sc[8];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) f2_unpack(s2[k], sc[2 * k], sc[2 * k + 1]);
+            const float sum = ((sc[0] + sc[1]) + (sc[2] + sc[3])) + ((sc[4] + sc[5]) + (sc[6] + sc[7]));
+            l_run = l_run * alpha + sum;
+            if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+                // With three S buffers, PV of the previous block may still be accumulating into O.
+                if (C::kThreeS && !(ok = prev_pv_done<D>(bars, t, j, T, wc))) break;
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t x[32];
+                    tmem_ld32(tO + q * 32, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) x[c] = __float_as_uint(__uint_as_float(x[c]) * alpha);
+                    tmem_st32(tO + q * 32, x);
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            mbar_arrive(&bars->p_full[t][j & 1]);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(&bars->p_full[t][j & 1]);
     }
     if (!ok) return;
     if (!warp_wait(&bars->o_full[t], 0, wc)) return;
