@@ -43,8 +43,7 @@
 // tile, then its dS^T (once dV has read dO), then the first warpgroup's fp32 dQ columns (once dQ has read
 // dS^T) as d / 64 [128][32] blocks, 128-byte swizzled and written with 16-byte stores; the TMA thread adds
 // each block into the accumulator with one tensor reduce and loads the dO tile of step i + 2 there by
-// 64-column chunks, each once the block under it has been read; the MMA thread starts dP^T(i+2) on the
-// first chunk.  The second warpgroup's blocks have a buffer of their own.  The kernel has no static shared
+// 64-column chunks, each once the block under it has been read (one barrier for the whole tile).  The second warpgroup's blocks have a buffer of their own.  The kernel has no static shared
 // memory, so its dynamic region starts aligned and needs no slack.
 //
 // (An earlier layout formed dQ^T = K^T dS^T at d = 128, thread = head-dimension index, each warp staging a
@@ -75,7 +74,7 @@ struct BwdBarriers {
     uint64_t kv_full;
     uint64_t q_full[2];            // Q tile + LSE2 and -D rows of a step
     uint64_t q_empty[2];           // dK of that step has read the Q tile
-    uint64_t do_full[2][2];        // [slot][64-column chunk]: that chunk of a step's dO tile is in its slot
+    uint64_t do_full[2];           // a step's dO tile is in its slot
     uint64_t dv_done[2];           // dV of that step has read dO: the slot takes dS^T
     uint64_t staged_a[2];          // the first warpgroup's dQ columns are staged in the slot
     uint64_t s_full;
@@ -205,8 +204,8 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
                 if (C::kChunks == 2 && c == 0) bulk_wait_group_read<1>();
                 else bulk_wait_group_read<0>();
             }
-            mbar_expect_tx(&bars->do_full[s][c], C::kChunkQ);
-            tma_load_3d(smem + C::kOffSlot + s * C::kSlotBytes + c * C::kChunkQ, tm_do, &bars->do_full[s][c], c * 64,
+            if (c == 0) mbar_expect_tx(&bars->do_full[s], C::kQBytes);
+            tma_load_3d(smem + C::kOffSlot + s * C::kSlotBytes + c * C::kChunkQ, tm_do, &bars->do_full[s], c * 64,
                         qb * BQ, head, pol_keep);
         }
         do_issued = i + 1;
@@ -217,7 +216,7 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
     drain_wait(&bars->kv_full, 0, wc);
     for (int i = (q_issued > 2 ? q_issued - 2 : 0); i < q_issued; ++i) drain_wait(&bars->q_full[i & 1], (i >> 1) & 1, wc);
     for (int i = (do_issued > 2 ? do_issued - 2 : 0); i < do_issued; ++i)
-        for (int c = 0; c < C::kChunks; ++c) drain_wait(&bars->do_full[i & 1][c], (i >> 1) & 1, wc);
+        drain_wait(&bars->do_full[i & 1], (i >> 1) & 1, wc);
 }
 
 // MMA order of step i: dV(i), S^T(i+1), dK(i), dQ(i), dP^T(i+1).  S^T of the next step goes right
@@ -267,34 +266,15 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
             mma_ss(d, sdesc_advance(ds0, kk * 16 * 128), sdesc_advance(mK, kk * 16 * 128), idQ, kk > 0);
     };
 
-    // dP^T = V dO^T for the dO tile in `slot`, one 64-column chunk of the head dimension (four k-steps) at
-    // a time: chunk 0 has been waited for by the caller; each further chunk is waited for here, so the
-    // first k-steps run while the rest of the tile is still landing.
-    auto dp_by_chunks = [&](int slot, uint32_t ph) -> bool {
-        const uint64_t b0 = sdesc_advance(kDO, slot * C::kSlotBytes);
-        const uint32_t d = tmem + C::kColDP;
-#pragma unroll
-        for (int c = 0; c < C::kChunks; ++c) {
-            if (c > 0) {
-                if (!mbar_wait_poll(&bars->do_full[slot][c], ph, wc)) return false;
-                tc_fence_after();
-            }
-#pragma unroll
-            for (int kk = 4 * c; kk < 4 * c + 4; ++kk)
-                mma_ss(d, sdesc_advance(kV, (kk / 4) * C::kChunkK + (kk % 4) * 32),
-                       sdesc_advance(b0, (kk / 4) * C::kChunkQ + (kk % 4) * 32), idS, kk > 0);
-        }
-        return true;
-    };
-
     bool ok = mbar_wait_poll(&bars->kv_full, 0, wc) && mbar_wait_poll(&bars->q_full[0], 0, wc);
     if (ok) {
         tc_fence_after();
         qk_like(kK, kQ, C::kColS);
         mma_commit(&bars->s_full);
-        if ((ok = mbar_wait_poll(&bars->do_full[0][0], 0, wc))) {
+        if ((ok = mbar_wait_poll(&bars->do_full[0], 0, wc))) {
             tc_fence_after();
-            if ((ok = dp_by_chunks(0, 0))) mma_commit(&bars->dp_full);
+            qk_like(kV, kDO, C::kColDP);
+            mma_commit(&bars->dp_full);
         }
     }
     for (int i = 0; ok && i < Tq; ++i) {
@@ -332,11 +312,13 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
         dq(sdesc_advance(mDS, s * C::kSlotBytes));
         mma_commit(&bars->dq_full);
         if (i + 1 < Tq) {
-            if (!(ok = mbar_wait_poll(&bars->do_full[s1][0], ((i + 1) >> 1) & 1, wc))) break;
+            // One test for the whole dO tile: testing its two 64-column chunks separately, so that dP^T
+            // could start on the first, measured 1.1-1.5 % slower at d = 128.
+            if (!(ok = mbar_wait_poll(&bars->do_full[s1], ((i + 1) >> 1) & 1, wc))) break;
             // At d = 128 the columns of dP^T hold dQ of step i until it has been moved out.
             if (!C::kOwnDQ && !(ok = mbar_wait_poll(&bars->dq_empty, i & 1, wc))) break;
             tc_fence_after();
-            if (!(ok = dp_by_chunks(s1, ((i + 1) >> 1) & 1))) break;
+            qk_like(kV, sdesc_advance(kDO, s1 * C::kSlotBytes), C::kColDP);
             mma_commit(&bars->dp_full);
         }
     }
@@ -538,8 +520,7 @@ bwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         for (int t = 0; t < 2; ++t) {
             mbar_init(&bars->q_full[t], 1);
             mbar_init(&bars->q_empty[t], 1);
-            mbar_init(&bars->do_full[t][0], 1);
-            mbar_init(&bars->do_full[t][1], 1);
+            mbar_init(&bars->do_full[t], 1);
             mbar_init(&bars->dv_done[t], 1);
             mbar_init(&bars->staged_a[t], 128);
             mbar_init(&bars->ds_ready[t], 128);
