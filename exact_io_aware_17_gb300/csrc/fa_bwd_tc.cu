@@ -116,12 +116,12 @@ struct BwdCfg {
     static constexpr uint32_t kOffStageB = kOffSlot + 2 * kSlotBytes;   // the second half's dQ rows
     // A warpgroup's dQ columns are staged as [BQ][32] fp32 blocks (128-byte swizzled, written by 16-byte
     // stores), d / 64 of them, each added into the accumulator by one tensor reduce.
-    static constexpr int kStripes = D / 64;
+    static constexpr int kDqBlocks = D / 64;
     // d = 64: dS ready for dK (tensor memory) is signalled before the shared-memory copy for dQ, which
     // waits for dV to have read the slot; a barrier of its own covers that copy.  At d = 128 one signal
     // after both measured as fast (and 0.7 % faster at N = 32768).
     static constexpr bool kEarlyDsReady = D == 64;
-    static constexpr uint32_t kStripeBytes = BQ * 32 * 4;
+    static constexpr uint32_t kDqBlockBytes = BQ * 32 * 4;
     static constexpr uint32_t kRowBytes = BQ * 4;          // LSE2 or -D of one query block
     static constexpr uint32_t kOffRows = kOffStageB + kHalfDQBytes;    // [q stage][LSE2 | -D][BQ] floats
     static constexpr uint32_t kOffBar = kOffRows + 2 * 2 * kRowBytes;
@@ -138,7 +138,7 @@ struct BwdCfg {
     static_assert(kColDQ + D <= 512, "tensor memory columns");
     static constexpr uint32_t kTmemCols = 512;
     static_assert(kQBytes <= kSlotBytes && kHalfDQBytes <= kSlotBytes, "slot contents");
-    static_assert(kStripes * kStripeBytes == kHalfDQBytes && kStripes == kChunks, "one block per dO chunk");
+    static_assert(kDqBlocks * kDqBlockBytes == kHalfDQBytes && kDqBlocks == kChunks, "one block per dO chunk");
     static_assert(kSmemNeed <= 232448, "shared memory per CTA");
 };
 
@@ -170,8 +170,8 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         const int t = j & 1;
         const int q0 = qblock(j, rot, Tq) * BQ;
         if (!mbar_wait(&bars->staged_a[t], (j >> 1) & 1, wc)) return false;
-        for (int w = 0; w < C::kStripes; ++w) {
-            tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kStripeBytes, 32 * w, q0, head);
+        for (int w = 0; w < C::kDqBlocks; ++w) {
+            tma_reduce_add_3d(tm_dq, smem + C::kOffSlot + t * C::kSlotBytes + w * C::kDqBlockBytes, 32 * w, q0, head);
             bulk_commit_group();
         }
         return true;
@@ -451,13 +451,13 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         for (int b = 0; b < D / 64; ++b)
 #pragma unroll
             for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4*>(rowp + b * C::kStripeBytes + ((j ^ (lane & 7)) << 4)) =
+                *reinterpret_cast<uint4*>(rowp + b * C::kDqBlockBytes + ((j ^ (lane & 7)) << 4)) =
                     make_uint4(x[b][4 * j], x[b][4 * j + 1], x[b][4 * j + 2], x[b][4 * j + 3]);
         fence_proxy_async_smem();
         mbar_arrive(half == 0 ? &bars->staged_a[s] : &bars->staged_b);
         if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
             for (int b = 0; b < D / 64; ++b)
-                tma_reduce_add_3d(tm_dq, smem + C::kOffStageB + b * C::kStripeBytes, D / 2 + 32 * b,
+                tma_reduce_add_3d(tm_dq, smem + C::kOffStageB + b * C::kDqBlockBytes, D / 2 + 32 * b,
                                   qblock(i, rot, Tq) * BQ, head);
             bulk_commit_group();
         }
