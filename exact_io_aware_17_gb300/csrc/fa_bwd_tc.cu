@@ -36,15 +36,18 @@
 // (tensor-memory lanes) and split each step's queries, 64 each, for P^T and dS^T; for dQ the lanes are
 // the step's 128 queries and the warpgroups split the head dimension, d / 2 columns each, which they move
 // out of tensor memory (thread = query row) and stage.  At the end warps 0-3 write dV and warps 4-7 dK.
-// Warp 8 issues the TMA loads and the first warpgroup's reduce-adds, warp 9 allocates tensor memory and
-// issues the MMAs; the second warpgroup's reduce-adds come from its own leader thread.
+// Warp 8 issues the TMA loads and every reduce-add, warp 9 allocates tensor memory and issues the MMAs.
 //
 // Shared memory (d = 128: 226 KB): K and V resident, two Q stages, and two slots that each hold a step's dO
 // tile, then its dS^T (once dV has read dO), then the first warpgroup's fp32 dQ columns (once dQ has read
 // dS^T) as d / 64 [128][32] blocks, 128-byte swizzled and written with 16-byte stores; the TMA thread adds
 // each block into the accumulator with one tensor reduce and loads the dO tile of step i + 2 there by
-// 64-column chunks, each once the block under it has been read (one barrier for the whole tile).  The second warpgroup's blocks have a buffer of their own.  The kernel has no static shared
-// memory, so its dynamic region starts aligned and needs no slack.
+// 64-column chunks, each once the block under it has been read (one barrier for the whole tile).  The
+// second warpgroup's blocks have a buffer of their own, which the TMA thread adds only after it has issued
+// that dO load: the copy engine serves bulk copies in issue order, and with the second half's reduce
+// issued first (from that warpgroup's own leader thread) the dO tile waited behind it, 11 % of the
+// backward at d = 128.  The kernel has no static shared memory, so its dynamic region starts aligned and
+// needs no slack.
 //
 // (An earlier layout formed dQ^T = K^T dS^T at d = 128, thread = head-dimension index, each warp staging a
 // [64][32] stripe with scalar stores: once the tensor-memory loads were widened to 64 columns, the present
@@ -84,8 +87,8 @@ struct BwdBarriers {
     uint64_t ds_smem;              // d = 64: both halves' dS^T are in the step's slot (what dQ reads)
     uint64_t dq_full;
     uint64_t dq_empty;
-    uint64_t staged_b;             // the second half's dQ rows are in their staging buffer
-    uint64_t stage_b_free;         // ... and their reduce has read them
+    uint64_t staged_b;             // the second warpgroup's dQ columns are in their staging buffer
+    uint64_t stage_b_free;         // ... and their reduce has read them (arrived by the TMA thread)
     uint64_t dkdv_full;
     uint64_t mma_done;
     uint32_t tmem_base;
@@ -176,6 +179,20 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
         }
         return true;
     };
+    // The second warpgroup's dQ columns of step j, from their own buffer, added after the dO loads so that
+    // those do not queue behind them; the buffer is handed back once the reduce has read it.
+    auto reduce_second_half = [&](int j) -> bool {
+        if (!mbar_wait(&bars->staged_b, j & 1, wc)) return false;
+        const int q0 = qblock(j, rot, Tq) * BQ;
+        for (int b = 0; b < C::kDqBlocks; ++b)
+            tma_reduce_add_3d(tm_dq, smem + C::kOffStageB + b * C::kDqBlockBytes, D / 2 + 32 * b, q0, head);
+        bulk_commit_group();
+        return true;
+    };
+    auto free_stage_b = [&]() {
+        bulk_wait_group_read<0>();
+        mbar_arrive(&bars->stage_b_free);
+    };
     int q_issued = 0, do_issued = 0;
     bool ok = true;
     for (int i = 0; i < Tq && ok; ++i) {
@@ -197,7 +214,10 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
             q_issued = i + 1;
         }
 
-        if (i >= 2 && !(ok = reduce_first_half(i - 2))) break;
+        if (i >= 2) {
+            if (i >= 3) free_stage_b();
+            if (!(ok = reduce_first_half(i - 2))) break;
+        }
         for (int c = 0; c < C::kChunks; ++c) {
             // Chunk c overwrites the block of reduce group c (the groups are read in order).
             if (i >= 2) {
@@ -209,8 +229,12 @@ __device__ void bwd_producer(const CUtensorMap* tm_q, const CUtensorMap* tm_k, c
                         qb * BQ, head, pol_keep);
         }
         do_issued = i + 1;
+        if (i >= 2 && !(ok = reduce_second_half(i - 2))) break;
     }
-    for (int j = (Tq > 2 ? Tq - 2 : 0); ok && j < Tq; ++j) ok = reduce_first_half(j);
+    for (int j = (Tq > 2 ? Tq - 2 : 0); ok && j < Tq; ++j) {
+        if (j >= 1) free_stage_b();
+        ok = reduce_first_half(j) && reduce_second_half(j);
+    }
     bulk_wait_group<0>();
     // Copies still in flight must land before the CTA can exit.
     drain_wait(&bars->kv_full, 0, wc);
@@ -342,7 +366,6 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
     const int r = quarter * 32 + lane;                    // key row in the block, = TMEM lane
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const bool valid_key = k0 + r < N;
-    const bool leader = (threadIdx.x % 128) == 0;
     const float* rows_base = reinterpret_cast<const float*>(smem + C::kOffRows);
     const uint64_t sl2 = f2_pack(scale_log2, scale_log2);
 
@@ -439,13 +462,7 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
         tmem_ld_wait();
         tc_fence_before();
         if constexpr (!C::kOwnDQ) mbar_arrive(&bars->dq_empty);
-        if (half == 1 && i > 0) {
-            if (leader) {
-                bulk_wait_group_read<0>();
-                mbar_arrive(&bars->stage_b_free);
-            }
-            if (!(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
-        }
+        if (half == 1 && i > 0 && !(ok = warp_wait(&bars->stage_b_free, (i - 1) & 1, wc))) break;
         uint8_t* rowp = smem + (half == 0 ? C::kOffSlot + s * C::kSlotBytes : C::kOffStageB) + r * 128;
 #pragma unroll
         for (int b = 0; b < D / 64; ++b)
@@ -455,14 +472,7 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
                     make_uint4(x[b][4 * j], x[b][4 * j + 1], x[b][4 * j + 2], x[b][4 * j + 3]);
         fence_proxy_async_smem();
         mbar_arrive(half == 0 ? &bars->staged_a[s] : &bars->staged_b);
-        if (half == 1 && leader && mbar_wait(&bars->staged_b, i & 1, wc)) {
-            for (int b = 0; b < D / 64; ++b)
-                tma_reduce_add_3d(tm_dq, smem + C::kOffStageB + b * C::kDqBlockBytes, D / 2 + 32 * b,
-                                  qblock(i, rot, Tq) * BQ, head);
-            bulk_commit_group();
-        }
     }
-    if (leader) bulk_wait_group<0>();
     if (!ok) return;
     if (!warp_wait(&bars->dkdv_full, 0, wc)) return;
     tc_fence_after();
