@@ -676,7 +676,7 @@ cudaError_t launch(const void* q, const void* k, const void* v, const void* o, c
     if ((e = make_tmap_bf16_3d(&tdo, dout, s.d, s.N, s.heads(), BQ)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tk, k, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
     if ((e = make_tmap_bf16_3d(&tv, v, s.d, s.N, s.heads(), BK)) != cudaSuccess) return e;
-    // The dQ staging boxes: [HQ rows][32 columns] unswizzled (d = 128), [BQ rows][32 columns] swizzled (d = 64).
+    // The dQ staging boxes: [BQ rows][32 columns], 128-byte swizzled.
     if ((e = make_tmap_f32_3d(&tdq, dq_acc, s.d, s.N, s.heads(), 32, BQ, true)) != cudaSuccess)
         return e;
     e = set_max_dynamic_smem((const void*)bwd_tc_kernel<D>, (int)C::kSmemBytes);
