@@ -399,11 +399,11 @@ def _e2e(fa, w, inp_cpu, dev, steps):
 # stale: the JSON line then reports traffic null and says so.
 TRAFFIC = {
     ("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): {
-        "bytes": 202488064 + 82951936,
+        "bytes": 202762496 + 82028800,
         "profile": "profiles/dram_per_launch_bench_B1-H16-N8192-d128.md",
         "kernel": "bwd_tc_kernel<128>",
         "sources": ("exact_io_aware_17_gb300/csrc/fa_bwd_tc.cu", "exact_io_aware_17_gb300/csrc/fa_ptx.cuh"),
-        "sha256": "4ea1dbfbd52ad2787ce37f61f29b076a12e246286db8a55278ea7102b9b9ea78",
+        "sha256": "4ec07c32e223a7ffc6c9ce0fd1df79023fbb650a4d38eeea6535aa10a66a150c",
     },
 }
 
