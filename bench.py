@@ -327,7 +327,8 @@ def run_ours(args, w):
 
 def _e2e(fa, w, inp_cpu, dev, steps):
     """Per-step time of fa_fwd + fa_bwd fed from and drained to pinned host memory, double-buffered: step i's
-    inputs are copied in while step i-1 computes, and its outputs copied out while step i+1 computes.  Every
+    inputs are copied in while step i-1 computes, and its outputs copied out while step i+1 computes (o and
+    lse already while step i's backward runs; step i's backward waits for dO, its forward does not).  Every
     tensor has a copy stream of its own, so that the copies of a step use several copy engines at once."""
     B, H, N, d = w.B, w.H, w.N, w.d
     ins, outs = ("q", "k", "v", "do"), ("o", "lse", "dq", "dk", "dv")
@@ -346,6 +347,7 @@ def _e2e(fa, w, inp_cpu, dev, steps):
     s_in = {n: torch.cuda.Stream(dev) for n in ins}
     s_out = {n: torch.cuda.Stream(dev) for n in outs}
     computed = [torch.cuda.Event() for _ in range(2)]          # buffer j's inputs read, outputs written
+    fwd_done = [torch.cuda.Event() for _ in range(2)]          # buffer j's o and lse written
     loaded = [{n: torch.cuda.Event() for n in ins} for _ in range(2)]
     drained = [{n: torch.cuda.Event() for n in outs} for _ in range(2)]
     for j in range(2):
@@ -353,30 +355,36 @@ def _e2e(fa, w, inp_cpu, dev, steps):
         for e in drained[j].values():
             e.record(comp)
 
+    def drain(j, names, after):
+        for name in names:
+            st = s_out[name]
+            st.wait_event(after)
+            with torch.cuda.stream(st):
+                host_out[j][name].copy_(bufs[j][name], non_blocking=True)
+                drained[j][name].record(st)
+
     def run(n):
         for i in range(n):
             j = i % 2
-            b, ho = bufs[j], host_out[j]
+            b = bufs[j]
             for name in ins:                               # buffer j's inputs are free once step i-2 computed
                 st = s_in[name]
                 st.wait_event(computed[j])
                 with torch.cuda.stream(st):
                     b[name].copy_(host_in[name], non_blocking=True)
                     loaded[j][name].record(st)
-            for name in ins:
+            for name in ("q", "k", "v"):
                 comp.wait_event(loaded[j][name])
             for name in outs:                              # ... and its outputs once step i-2's were copied out
                 comp.wait_event(drained[j][name])
             fa.fa_fwd(b["q"], b["k"], b["v"], w.scale, b["o"], b["lse"], stream=comp)
+            fwd_done[j].record(comp)
+            drain(j, ("o", "lse"), fwd_done[j])            # final after the forward: out while the backward runs
+            comp.wait_event(loaded[j]["do"])               # dO is needed only from here on
             fa.fa_bwd(b["q"], b["k"], b["v"], b["o"], b["do"], b["lse"], w.scale, b["dq"], b["dk"], b["dv"], b["ws"],
                       stream=comp)
             computed[j].record(comp)
-            for name in outs:
-                st = s_out[name]
-                st.wait_event(computed[j])
-                with torch.cuda.stream(st):
-                    ho[name].copy_(b[name], non_blocking=True)
-                    drained[j][name].record(st)
+            drain(j, ("dq", "dk", "dv"), computed[j])
 
     run(4)
     torch.cuda.synchronize(dev)
