@@ -44,9 +44,8 @@
 // each block into the accumulator with one tensor reduce and loads the dO tile of step i + 2 there by
 // 64-column chunks, each once the block under it has been read (one barrier for the whole tile).  The
 // second warpgroup's blocks have a buffer of their own, which the TMA thread adds only after it has issued
-// that dO load: the copy engine serves bulk copies in issue order, and with the second half's reduce
-// issued first (from that warpgroup's own leader thread) the dO tile waited behind it, 11 % of the
-// backward at d = 128.  The kernel has no static shared memory, so its dynamic region starts aligned and
+// that dO load: with the second half's reduce issued first (from that warpgroup's own leader thread) the dO
+// tile queued behind it in the copy unit, which cost 11 % of the backward at d = 128.  The kernel has no static shared memory, so its dynamic region starts aligned and
 // needs no slack.
 //
 // (An earlier layout formed dQ^T = K^T dS^T at d = 128, thread = head-dimension index, each warp staging a
