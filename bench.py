@@ -407,11 +407,11 @@ def _e2e(fa, w, inp_cpu, dev, steps):
 # stale: the JSON line then reports traffic null and says so.
 TRAFFIC = {
     ("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): {
-        "bytes": 202624256 + 81988608,
+        "bytes": 203081984 + 84119296,
         "profile": "profiles/dram_per_launch_bench_B1-H16-N8192-d128.md",
         "kernel": "bwd_tc_kernel<128>",
         "sources": ("exact_io_aware_17_gb300/csrc/fa_bwd_tc.cu", "exact_io_aware_17_gb300/csrc/fa_ptx.cuh"),
-        "sha256": "4aa8c12703ce51217e65ebfe44c29cddf4d1292b6c8dfea5a00d895f48227263",
+        "sha256": "0c7bec96d6d25f612b1aa7efd6ffe34f07b9a83314cd5dfe25508613da24b0df",
     },
 }
 
