@@ -375,7 +375,6 @@ __device__ void softmax_wg(FwdBarriers* bars, uint32_t tmem, int t, __nv_bfloat1
             // s * scale*log2e - m and the row sum run on packed pairs (f32x2): two results per instruction.
             const uint64_t sl2 = f2_pack(scale_log2, scale_log2), nm2 = f2_pack(neg_m, neg_m);
             uint64_t s2[4] = {0, 0, 0, 0};
-#pragma unroll
             // P of keys [64 h, 64 h + 64) as 32 bf16 pairs.
             auto exp_half = [&](int h, uint32_t (&pk)[32]) {
 #pragma unroll
