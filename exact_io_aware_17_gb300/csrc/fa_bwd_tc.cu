@@ -45,8 +45,8 @@
 // 64-column chunks, each once the block under it has been read (one barrier for the whole tile).  The
 // second warpgroup's blocks have a buffer of their own, which the TMA thread adds only after it has issued
 // that dO load: with the second half's reduce issued first (from that warpgroup's own leader thread) the dO
-// tile queued behind it in the copy unit, which cost 11 % of the backward at d = 128.  At d = 128 the K and V
-// tiles' space takes the bf16 rows of dK and dV at the end, so that they leave in whole-row stores.  The kernel has no static shared memory, so its dynamic region starts aligned and
+// tile queued behind it in the copy unit, which cost 11 % of the backward at d = 128.  At the end the K and V
+// tiles' space takes the bf16 rows of dK and dV, so that they leave in whole-row stores.  The kernel has no static shared memory, so its dynamic region starts aligned and
 // needs no slack.
 //
 // (An earlier layout formed dQ^T = K^T dS^T at d = 128, thread = head-dimension index, each warp staging a
@@ -352,6 +352,57 @@ __device__ void bwd_mma(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, int Tq)
     drain_wait(&bars->mma_done, 0, wc);
 }
 
+// Warps 0-7 write dV (0-3) and dK (4-7, scaled) once every MMA has completed.  The K and V tiles are free
+// by then: each thread converts its key row to bf16 and puts it in the V (dV) or K (dK) tile's space,
+// 16-byte chunks XOR-swizzled by the row; then each warp copies its own 32 rows out, a warp's 16-byte
+// stores covering whole rows (two at d = 128, four at d = 64), where one row per thread would touch 32
+// rows of memory per store.  A call rather than inlined code: inlined, its registers shaped the step loop
+// of bwd_softgrad (this copy inlined made the d = 64 backward 2.4 % slower; called, it is 1.5-1.8 % faster
+// than the one-row-per-thread stores at every N, and at d = 128 0.3 % faster at N = 8192, 1.8 % at 2048).
+template <int D>
+__device__ __noinline__ void bwd_write_dkdv(uint8_t* smem, uint32_t tmem, __nv_bfloat16* __restrict__ dk,
+                                                   __nv_bfloat16* __restrict__ dv, int head, int k0, int N, float scale) {
+    using C = BwdCfg<D>;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+    const int half = warp / 4, quarter = warp % 4;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
+    const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
+    const float mul = half == 0 ? 1.f : scale;
+    __nv_bfloat16* out = half == 0 ? dv : dk;
+    uint8_t* tile = smem + (half == 0 ? C::kOffV : C::kOffK);
+    constexpr int kRowChunks = D / 8;                 // 16-byte chunks in a bf16 row
+    constexpr int kRowsPerStore = 32 / kRowChunks;    // rows one warp store covers
+#pragma unroll
+    for (int q2 = 0; q2 < D / 64; ++q2) {
+        uint32_t y[2][32];
+        tmem_ld64(tmem + lane_off + col + q2 * 64, y);
+        tmem_ld_wait();
+#pragma unroll
+        for (int b = 0; b < 2; ++b)
+#pragma unroll
+            for (int c4 = 0; c4 < 4; ++c4) {
+                const int c = q2 * 8 + b * 4 + c4;
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    w[e] = pack_bf16(__uint_as_float(y[b][8 * c4 + 2 * e]) * mul,
+                                     __uint_as_float(y[b][8 * c4 + 2 * e + 1]) * mul);
+                *reinterpret_cast<uint4*>(tile + r * (D * 2) + ((c ^ (r & (kRowChunks - 1))) << 4)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
+            }
+    }
+    __syncwarp();
+    const int sub = lane / kRowChunks, c = lane % kRowChunks;
+#pragma unroll
+    for (int it = 0; it < 32 / kRowsPerStore; ++it) {
+        const int rr = quarter * 32 + it * kRowsPerStore + sub;
+        const uint4 v = *reinterpret_cast<const uint4*>(tile + rr * (D * 2) + ((c ^ (rr & (kRowChunks - 1))) << 4));
+        if (k0 + rr < N)
+            *reinterpret_cast<uint4*>(out + ((size_t)head * N + k0 + rr) * D + c * 8) = v;
+    }
+}
+
 // Warps 0-7.  Thread = key row r of the CTA (tensor-memory lane) in the softmax-gradient part, where
 // `half` selects queries [64 half, 64 half + 64) of each step, and query row r of the step in the dQ
 // part, where `half` selects head-dimension columns [d/2 half, d/2 half + d/2).
@@ -499,70 +550,7 @@ __device__ void bwd_softgrad(uint8_t* smem, BwdBarriers* bars, uint32_t tmem, fl
     if (!ok) return;
     if (!warp_wait(&bars->dkdv_full, 0, wc)) return;
     tc_fence_after();
-    // Warps 0-3 write dV, warps 4-7 dK (scaled).
-    if constexpr (D == 128) {
-        // Every MMA has completed, so the K and V tiles are free: each thread converts its key row to bf16
-        // and puts it in the V (dV) or K (dK) tile's space, 16-byte chunks XOR-swizzled by the row; then
-        // each warp copies its own 32 rows out, a warp's 16-byte stores covering two whole rows.  Storing
-        // one row per thread touches 32 rows of memory per store; this copy measured 0.3 % faster at
-        // N = 8192 and 1.8 % at N = 2048.  At d = 64 the same code made the whole backward 2.4 % slower.
-        const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
-        const float mul = half == 0 ? 1.f : scale;
-        __nv_bfloat16* out = half == 0 ? dv : dk;
-        uint8_t* tile = smem + (half == 0 ? C::kOffV : C::kOffK);
-        constexpr int kRowChunks = D / 8;                 // 16-byte chunks in a bf16 row
-        constexpr int kRowsPerStore = 32 / kRowChunks;    // rows one warp store covers
-#pragma unroll
-        for (int q2 = 0; q2 < D / 64; ++q2) {
-            uint32_t y[2][32];
-            tmem_ld64(tmem + lane_off + col + q2 * 64, y);
-            tmem_ld_wait();
-#pragma unroll
-            for (int b = 0; b < 2; ++b)
-#pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    const int c = q2 * 8 + b * 4 + c4;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        w[e] = pack_bf16(__uint_as_float(y[b][8 * c4 + 2 * e]) * mul,
-                                         __uint_as_float(y[b][8 * c4 + 2 * e + 1]) * mul);
-                    *reinterpret_cast<uint4*>(tile + r * (D * 2) + ((c ^ (r & (kRowChunks - 1))) << 4)) =
-                        make_uint4(w[0], w[1], w[2], w[3]);
-                }
-        }
-        __syncwarp();
-        const int sub = lane / kRowChunks, c = lane % kRowChunks;
-#pragma unroll
-        for (int it = 0; it < 32 / kRowsPerStore; ++it) {
-            const int rr = quarter * 32 + it * kRowsPerStore + sub;
-            const uint4 v = *reinterpret_cast<const uint4*>(tile + rr * (D * 2) + ((c ^ (rr & (kRowChunks - 1))) << 4));
-            if (k0 + rr < N)
-                *reinterpret_cast<uint4*>(out + ((size_t)head * N + k0 + rr) * D + c * 8) = v;
-        }
-    } else {
-        // Each thread its key row.
-        const uint32_t col = half == 0 ? C::kColDV : C::kColDK;
-        const float mul = half == 0 ? 1.f : scale;
-        __nv_bfloat16* out = half == 0 ? dv : dk;
-        const size_t base = ((size_t)head * N + k0 + r) * D;
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-            uint32_t y[32];
-            tmem_ld32(tmem + lane_off + col + q * 32, y);
-            tmem_ld_wait();
-            uint32_t pk2[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c)
-                pk2[c] = pack_bf16(__uint_as_float(y[2 * c]) * mul, __uint_as_float(y[2 * c + 1]) * mul);
-            if (valid_key) {
-                uint4* dst = reinterpret_cast<uint4*>(out + base + q * 32);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    dst[c] = make_uint4(pk2[4 * c], pk2[4 * c + 1], pk2[4 * c + 2], pk2[4 * c + 3]);
-            }
-        }
-    }
+    bwd_write_dkdv<D>(smem, tmem, dk, dv, head, k0, N, scale);
 }
 
 template <int D>
