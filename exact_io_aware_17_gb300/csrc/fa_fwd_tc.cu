@@ -30,7 +30,11 @@
 // cluster streams half of the K/V blocks, rank 1 hands its unnormalised O, m and l to rank 0 through
 // distributed shared memory, and rank 0 merges the halves,
 //     m = max(m0, m1),  l = 2^(m0-m) l0 + 2^(m1-m) l1,  O = (2^(m0-m) O0 + 2^(m1-m) O1) / l,
-// the same exp-sum factorisation as the online rescale.  The last wave then takes half as long.
+// the same exp-sum factorisation as the online rescale.  The last wave then takes half as long.  The
+// clusters' launch is a programmatic dependent of the full waves' (every CTA releases it at its start), so
+// its CTAs take SMs as the full waves leave them instead of waiting for the whole first launch to drain:
+// the forward measured 1.1 % faster at N = 8192 d = 128, 3.3 % at N = 2048 and 4.5 % at B=4 H=16 N=2048
+// d = 64.
 //
 // TMEM columns at d = 128: S0/P0 [0,128), S1/P1 [128,256), O0 [256,384), O1 [384,512).  At d = 64 S rotates
 // through three buffers [0,128), [128,256), [256,384) (S of the next tile is formed while the softmax works
@@ -541,6 +545,9 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     const uint32_t rank = split ? cluster_ctarank() : 0;
     const int kv0 = split ? (int)rank * (T_all / 2) : 0;
     const int T = split ? (rank ? T_all - T_all / 2 : T_all / 2) : T_all;
+    // The split tail's launch may start on SMs that the full waves have left; it reads only the call's
+    // inputs and writes other rows than they do.
+    griddep_launch_dependents();
 
     if (threadIdx.x == 0) {
         bars->wait.budget = wait_budget;
@@ -603,6 +610,8 @@ fwd_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         tmem_dealloc(tmem, C::kTmemCols);
     }
     if (threadIdx.x == 0 && bars->wait.abort) atomicCAS(&g_fwd_status, 0, (int)FA_ERR_TIMEOUT);
+    // A split-tail CTA does not finish before the full waves have: what follows on the stream sees both.
+    if (threadIdx.x == 0) griddep_wait();
 }
 
 template <int D, bool kStepNorm>
@@ -640,13 +649,15 @@ cudaError_t launch(const void* q, const void* k, const void* v, void* o, float* 
         cfg.blockDim = dim3(kThreads);
         cfg.dynamicSmemBytes = C::kSmemBytes;
         cfg.stream = st;
-        cudaLaunchAttribute attr[1];
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = 2;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = grid > 0 ? 1 : 0;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = 2;
         e = cudaLaunchKernelEx(&cfg, fwd_tc_kernel<D, kStepNorm>, tq, tk, tv, out, lse, s.N, bph, (int)full, 2,
                                scale_log2, wp.budget_cycles, wp.starve);
         if (e != cudaSuccess) return e;

@@ -50,6 +50,24 @@ int device_sm_count();
 // made only when the limit has to rise).
 cudaError_t set_max_dynamic_smem(const void* func, int bytes);
 
+// Launches `kernel` with programmatic stream serialisation: it may start while the kernel ahead of it on
+// `st` is finishing, and must itself wait (griddepcontrol.wait) before it reads anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Encodes a TMA descriptor for a bf16 [heads, N, d] array (d innermost) with boxes of 64 columns x
 // `box_rows` rows x 1 head and 128-byte swizzling; rows beyond N read as zero.  Encoded maps are cached by
 // their arguments (address, shape, box), so repeated calls on the same buffers cost a table lookup.

@@ -112,6 +112,14 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
     }
 }
 
+// ---------------------------------------------------------------- dependent launches
+// A kernel launched with programmatic stream serialisation may start before the kernel ahead of it on the
+// stream has finished; it must wait here before it touches anything that kernel writes.  (In a kernel
+// launched normally this returns at once.)
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream, if launched that way, start as this one's CTAs finish.
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
