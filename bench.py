@@ -407,11 +407,11 @@ def _e2e(fa, w, inp_cpu, dev, steps):
 # stale: the JSON line then reports traffic null and says so.
 TRAFFIC = {
     ("backward", "bf16-fwdbwd-B1-H16-N8192-d128"): {
-        "bytes": 202837760 + 84335616,
+        "bytes": 202727168 + 83696896,
         "profile": "profiles/dram_per_launch_bench_B1-H16-N8192-d128.md",
         "kernel": "bwd_tc_kernel<128>",
         "sources": ("exact_io_aware_17_gb300/csrc/fa_bwd_tc.cu", "exact_io_aware_17_gb300/csrc/fa_ptx.cuh"),
-        "sha256": "88b76ea4ce4adc9ea93b8d94809da1dd92db0ab230bc00fd7200ad3ff7b8df28",
+        "sha256": "7fc13617fa9cb275a4b7a52b17bff2358760e1c09fbe4b6634bd6124d7860954",
     },
 }
 

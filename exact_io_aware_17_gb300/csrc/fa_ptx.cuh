@@ -117,7 +117,8 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity, const
 // stream has finished; it must wait here before it touches anything that kernel writes.  (In a kernel
 // launched normally this returns at once.)
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-// Lets the next kernel on the stream, if launched that way, start as this one's CTAs finish.
+// Lets the next kernel on the stream, if launched that way, start once every CTA of this one has executed
+// this (or exited) rather than when this one completes.
 __device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 // ---------------------------------------------------------------- TMA
