@@ -311,3 +311,26 @@ def test_main_kernel_timing_events_are_recorded_once():
     torch.cuda.synchronize()
     assert e0.elapsed_time(e1) == main_ms
     fa.fa_check_status()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_timing_events_between_dependent_launches_change_nothing(d):
+    """The main and dQ-conversion kernels start as programmatic dependents of the kernel before them; with
+    the timing events recorded between the kernels the call must give the same gradients (dK, dV bitwise,
+    dQ up to the order of its reduce-adds) as without."""
+    fa = need_gpu()
+    B, H, N = 2, 8, 2000      # ragged: the last key block of each head is partial
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed=82, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    o, lse = fa.fa_fwd(q, k, v)
+    dq0, dk0, dv0 = fa.fa_bwd(q, k, v, o, do, lse)
+    e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+    for e in (e0, e1):
+        e.record(torch.cuda.current_stream())
+    fa.fa_debug_time_bwd_main(e0, e1)
+    dq1, dk1, dv1 = fa.fa_bwd(q, k, v, o, do, lse)
+    torch.cuda.synchronize()
+    fa.fa_check_status()
+    assert torch.equal(dk0, dk1) and torch.equal(dv0, dv1)
+    rel = ((dq0.float() - dq1.float()).norm() / dq0.float().norm()).item()
+    assert rel < 1e-3
