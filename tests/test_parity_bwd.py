@@ -334,3 +334,37 @@ def test_timing_events_between_dependent_launches_change_nothing(d):
     assert torch.equal(dk0, dk1) and torch.equal(dv0, dv1)
     rel = ((dq0.float() - dq1.float()).norm() / dq0.float().norm()).item()
     assert rel < 1e-3
+
+
+def test_forward_and_backward_replay_from_a_cuda_graph():
+    """Both calls captured into one CUDA graph (their launches include programmatic dependents and the
+    forward's 2-CTA cluster tail) replay to the results of the same calls made eagerly."""
+    fa = need_gpu()
+    B, H, N, d = 1, 20, 2048, 128       # 160 tile pairs: one full wave of 152 plus a split tail of 8
+    inp = fa_inputs.make_inputs(B, H, N, d, "bf16", seed=83, with_grad=True)
+    q, k, v, do = (inp[n].cuda() for n in ("q", "k", "v", "do"))
+    scale = 1 / math.sqrt(d)
+    o0, lse0 = fa.fa_fwd(q, k, v, scale)
+    dq0, dk0, dv0 = fa.fa_bwd(q, k, v, o0, do, lse0, scale)
+    o, lse = torch.empty_like(q), torch.empty(B, H, N, dtype=torch.float32, device=q.device)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(fa.fa_bwd_workspace_size(B, H, N, d), dtype=torch.uint8, device=q.device)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):                # warm-up off the default stream, as graph capture wants
+        fa.fa_fwd(q, k, v, scale, o, lse)
+        fa.fa_bwd(q, k, v, o, do, lse, scale, dq, dk, dv, ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for t in (o, lse, dq, dk, dv):
+        t.zero_()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fa.fa_fwd(q, k, v, scale, o, lse)
+        fa.fa_bwd(q, k, v, o, do, lse, scale, dq, dk, dv, ws)
+    g.replay()
+    torch.cuda.synchronize()
+    fa.fa_check_status()
+    assert torch.equal(o, o0) and torch.equal(lse, lse0)
+    assert torch.equal(dk, dk0) and torch.equal(dv, dv0)
+    assert rel_fro(np64(dq), np64(dq0)) < 1e-3
